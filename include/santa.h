@@ -1,0 +1,198 @@
+/*
+ * santa.h — C ABI of libsanta.so: SANTA++ decode-step attention on one GB300 (sm_103a).
+ *
+ * Sources of the method (cited by page title and section):
+ *   [ABS]  "SANTA++: Sampling Attention through Representative Keys" (arXiv 2609.35629),
+ *          abstract, as printed on arxivdaily.com and fugumt.com.
+ *   [EXP]  "SANTA++：用代表性 Key 采样把 KV cache 读带宽砍掉 80%" (papers.ananclaw.com
+ *          explainer), section 三 "core method", its five-step pipeline and 3.1.
+ *
+ * What the library computes, for every sequence b and KV head h (a "unit"):
+ *   teams      the n = ceil(seq_len/T) contiguous blocks of T cached tokens; team i is the
+ *              KV page page_table[b][i].                                   [ABS; EXP step 1]
+ *   reps       rep_i = mean of team i's valid keys (fp32 side buffer).     [ABS; EXP step 2]
+ *   probs      s_{g,i} = q_g . rep_i / sqrt(d) for the G = Hq/Hkv query heads g of the group;
+ *              p_{g,i} = softmax_i(s_{g,.});  p_i = (1/G) sum_g p_{g,i}.   [ABS; EXP step 2]
+ *   sampling   M i.i.d. draws with replacement from p; draw r uses Philox4x32-10 (Salmon et
+ *              al., SC'11) with key (lo32(seed), hi32(seed)) and counter (r, h, b, 0); word 0
+ *              x gives u = (x + 0.5) 2^-32, and the draw is the smallest i with u*Z < C_i,
+ *              C the running sum of p and Z = C_{n-1}.  S = the distinct drawn teams,
+ *              ascending; pi_i = 1 - (1 - p_i)^M.                          [ABS; EXP step 3]
+ *   attention  for each query head g of the group, the Horvitz-Thompson ratio
+ *              out_g = sum_{i in S} (1/pi_i) sum_{j in team i} e^{s_j} v_j
+ *                    / sum_{i in S} (1/pi_i) sum_{j in team i} e^{s_j},
+ *              s_j = q_g . k_j / sqrt(d).                               [ABS; EXP steps 4-5]
+ *
+ * Layouts (all row-major, all device memory unless stated):
+ *   q          [B][Hq][d]        dtype; query head hq reads KV head hq / G.
+ *   k_pool     [P][Hkv][T][d]    dtype; page p, head h is one contiguous T*d block.
+ *   v_pool     [P][Hkv][T][d]    dtype.
+ *   reps       [P][Hkv][d]       fp32.
+ *   page_table [B][max_teams]    int32, physical page of team i of sequence b.
+ *   seq_lens   [B]               int32, 1 <= seq_len <= max_teams*T.
+ *   out        [B][Hq][d]        fp32.
+ *   draw_ids   [B][Hkv][M]       int32, team index of every draw, in draw order.
+ *   sel_ids    [B][Hkv][M]       int32, S ascending, padded with -1.
+ *   sel_count  [B][Hkv]          int32, |S|.
+ *   pi         [B][Hkv][M]       fp32, pi_i aligned with sel_ids, padded with 0.
+ *   team_probs [B][Hkv][max_teams] fp32 (optional), p_i, padded with 0.
+ *
+ * Conventions:
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and runs on the device that is current on the calling thread.
+ *   - The caller owns and allocates every buffer.  The library allocates no memory and keeps
+ *     no per-call state; calls on different streams with disjoint buffers may overlap.
+ *   - Host-side argument errors return SANTA_ERR_INVALID_ARG / SANTA_ERR_UNSUPPORTED and
+ *     launch nothing.  A failed launch returns SANTA_ERR_CUDA.
+ *   - Errors only visible on the device (an out-of-range page id or seq_len) never trap:
+ *     the kernel ORs a SANTA_DEV_* bit into *device_status, skips the offending team or
+ *     unit (a skipped unit gets out = 0 and sel_count = 0) and carries on.  The caller
+ *     zeroes *device_status, synchronises and reads it; a non-zero word means the outputs
+ *     of the affected units are not meaningful (SANTA_ERR_DEVICE_STATUS).
+ *   - Supported shapes: dtype f32 or bf16; head_dim 64 or 128; team_size 64 or 128;
+ *     1 <= G <= 8; 1 <= M <= 4096; max_teams <= 16384.  All pointers 16-byte aligned.
+ */
+#ifndef SANTA_H
+#define SANTA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SANTA_ABI_VERSION 1
+
+typedef enum santa_status {
+  SANTA_OK = 0,
+  SANTA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, short workspace */
+  SANTA_ERR_UNSUPPORTED = 2,   /* a shape outside the supported set above */
+  SANTA_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+  SANTA_ERR_DEVICE_STATUS = 4  /* reserved for callers: *device_status was non-zero */
+} santa_status;
+
+typedef enum santa_dtype { SANTA_F32 = 0, SANTA_BF16 = 1 } santa_dtype;
+
+/* Bits ORed into *device_status by the kernels. */
+#define SANTA_DEV_BAD_PAGE 1u    /* a page id outside [0, num_pages) */
+#define SANTA_DEV_BAD_SEQLEN 2u  /* seq_len < 1 or seq_len > max_teams * team_size */
+#define SANTA_DEV_BAD_SEL 4u     /* santa_attend given a sel_ids/sel_count/pi entry out of range */
+
+/* Returns SANTA_ABI_VERSION of the loaded library. */
+int santa_abi_version(void);
+
+/* Static English text for a santa_status value (never NULL). */
+const char* santa_status_string(int status);
+
+/*
+ * santa_build_reps — the team representative of every (page, KV head): the mean of the
+ * page's valid keys.  [ABS: "the query scores one representative from each team";
+ * EXP section 三 step 2 lists the mean key as one choice of representative.]
+ *
+ *   k_pool      [num_pages][num_kv_heads][team_size][head_dim], dtype.
+ *   page_fill   [num_pages] int32 valid-token count of each page (0..team_size), or NULL
+ *               for "every page full".  A page with fill 0 gets a zero representative.
+ *   reps        [num_pages][num_kv_heads][head_dim] fp32, written.
+ *   device_status  one int32 (may be NULL); SANTA_DEV_BAD_SEQLEN if a fill is out of range.
+ * Run once after prefill; santa_update_reps refreshes single pages during decode.
+ */
+int santa_build_reps(const void* k_pool, int dtype, int64_t num_pages, int num_kv_heads,
+                     int team_size, int head_dim, const int32_t* page_fill, float* reps,
+                     int32_t* device_status, void* stream);
+
+/*
+ * santa_update_reps — recompute the representative of the listed pages only (for the pages
+ * that received new tokens during decode), with the same arithmetic as santa_build_reps.
+ *   pages [num_listed] int32 page ids (device); page_fill as in santa_build_reps (device,
+ *   indexed by page id, may be NULL for full pages).  A listed id out of range sets
+ *   SANTA_DEV_BAD_PAGE and is skipped.
+ */
+int santa_update_reps(const void* k_pool, int dtype, int64_t num_pages, int num_kv_heads,
+                      int team_size, int head_dim, const int32_t* pages, int num_listed,
+                      const int32_t* page_fill, float* reps, int32_t* device_status,
+                      void* stream);
+
+/* All inputs, outputs and scratch of one decode step (see the layouts above). */
+typedef struct santa_decode_args {
+  /* inputs */
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const float* reps;           /* read by santa_sample / santa_decode */
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int dtype;                   /* santa_dtype of q, k_pool and v_pool */
+  int batch;                   /* B */
+  int num_q_heads;             /* Hq */
+  int num_kv_heads;            /* Hkv, Hq % Hkv == 0 */
+  int head_dim;                /* d */
+  int team_size;               /* T, also the KV page size */
+  int max_teams;               /* row length of page_table */
+  int num_draws;               /* M */
+  int64_t num_pages;           /* P, rows of k_pool / v_pool / reps */
+  uint64_t seed;               /* Philox key */
+  /* outputs (santa_attend reads sel_ids, sel_count and pi as inputs) */
+  float* out;
+  int32_t* draw_ids;
+  int32_t* sel_ids;
+  int32_t* sel_count;
+  float* pi;
+  float* team_probs;           /* optional, may be NULL */
+  /* scratch: caller-owned device memory, contents need not be initialised */
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* device_status;      /* one int32 the kernels OR SANTA_DEV_* bits into */
+} santa_decode_args;
+
+/*
+ * Workspace for santa_attend / santa_decode: split-K partials (m, l, acc[d]) per query head
+ * and one arrival counter per unit.  Returns the size the library's default split plan
+ * uses on the current device; any smaller size of at least
+ * santa_decode_workspace_min_bytes still works, with fewer, longer splits.
+ */
+size_t santa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int team_size, int max_teams, int num_draws);
+size_t santa_decode_workspace_min_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                        int head_dim);
+
+/*
+ * santa_sample — score the representatives, form the GQA-mixed team distribution, draw M
+ * teams, deduplicate and compute the inclusion probabilities.  Writes draw_ids, sel_ids,
+ * sel_count, pi, team_probs (if not NULL) and resets the unit counters in the workspace.
+ * [ABS: "the query scores one representative from each team to decide which teams to
+ * sample"; EXP section 三 steps 2-3.]
+ */
+int santa_sample(const santa_decode_args* a, void* stream);
+
+/*
+ * santa_attend — exact attention inside the teams listed in sel_ids[0..sel_count) of every
+ * unit, each team weighted by 1/pi, combined as the Horvitz-Thompson ratio into out.
+ * sel_ids / sel_count / pi may come from santa_sample or from the caller (distinct team
+ * indices < n, any order, 0 < pi <= 1); entries out of range set SANTA_DEV_BAD_SEL and are
+ * skipped.  The workspace counters must have been reset by santa_sample on the same
+ * workspace, or the caller must zero the whole workspace first.
+ * [ABS: "We compute exact attention scores within the sampled teams and reweight each
+ * team's contribution by the inverse of its inclusion probability"; EXP steps 4-5.]
+ */
+int santa_attend(const santa_decode_args* a, void* stream);
+
+/* santa_decode — santa_sample followed by santa_attend on `stream`. [ABS] */
+int santa_decode(const santa_decode_args* a, void* stream);
+
+/*
+ * santa_dense_decode — exact dense softmax attention over all seq_len tokens of every
+ * sequence, split-K over the paged cache (the speed reference the sampled path is compared
+ * with; [ABS] compares against a dense FlashAttention baseline).  Reads q, k_pool, v_pool,
+ * page_table, seq_lens and the shape fields; writes out; uses workspace and device_status.
+ * reps, num_draws, seed and the sampling outputs are ignored.
+ */
+size_t santa_dense_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int team_size, int max_teams);
+int santa_dense_decode(const santa_decode_args* a, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SANTA_H */
