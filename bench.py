@@ -1,0 +1,478 @@
+#!/usr/bin/env python
+"""SANTA++ decode-step attention benchmark on GB300 — prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--cpu-seconds S] [--no-e2e]
+
+Workload: the Qwen2.5-7B-shaped decode attention layer at 32K context (1 sequence, 28 query
+/ 4 KV heads, d = 128, T = 128, M = 31 draws, bf16 K/V, mixture keys), seeded synthetic
+data.  A step is one SANTA++ decode step: team scoring + sampling (santa_sample's kernel)
+and the split-K Horvitz-Thompson attention (santa_attend's kernel), through santa_decode.
+
+value      steps/s of whole decode steps with inputs resident in HBM, K steps replayed from
+           CUDA graphs; the K/V/representative buffers rotate over R copies so that the
+           bytes touched between two uses of a copy exceed 6x the L2 size.
+roofline   the attention kernel (the dominant one): algorithmic bytes per launch (K and V of
+           the sampled teams, q, out) / its mean duration (CUDA events, graph-replayed
+           launches), against the measured HBM copy bandwidth.
+e2e        the same steps through the Python API with pinned host buffers: per step the
+           query, page table and lengths go host->device and out, draw/sampled ids, pi and
+           |S| come back device->host, then the stream is synchronised.
+dense      the in-run dense split-K decode kernel on the same buffers (speed reference).
+cpu_baseline  the fp64 C oracle, single-threaded, on a bounded sample of steps.
+--impl reference  times that oracle alone (the reference arm of this benchmark).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn steps/s and achieved HBM GB/s at 32K ctx, M=31/64 teams, 1 GB300"
+DEFAULT_WORKLOAD = "qwen7b_32k_b1_m31"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_traffic.json")
+ATTEND_SOURCES = ["sampled_sparse_decode_gb300/csrc/attend_kernel.cuh",
+                  "sampled_sparse_decode_gb300/csrc/common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attend_source_sha():
+    h = hashlib.sha256()
+    for rel in ATTEND_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on
+    the current kernel source and this workload (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_sha") == attend_source_sha() and rec.get("workload") == workload:
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms (read-only queries)."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 - 0.15 <= t <= t1 + 0.15] or \
+               [s for (_, s) in self.samples]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [x.strip() for x in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- oracle (CPU)
+
+def oracle_steps_per_s(wl, seconds, max_steps=None):
+    """The fp64 oracle, single-threaded, timed per decode step (reps precomputed)."""
+    import oracle
+    pr = oracle.Problem(wl.q, wl.k_pool, wl.v_pool, wl.page_table, wl.seq_lens)
+    reps = oracle.build_reps(pr, wl.page_fill)
+    cfg = wl.cfg
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        for b in range(cfg.batch):
+            for h in range(cfg.kv_heads):
+                oracle.decode(pr, reps, cfg.draws, steps, b, h)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_steps and steps >= max_steps):
+            return steps / el, steps, el
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, same workload and metric.  Each
+    step decodes a bounded sample of the step's (sequence, KV head) units, sized so that the
+    whole run takes about two minutes, and the time is scaled to whole steps."""
+    world, rank, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import oracle
+    from sampled_sparse_decode_gb300 import workloads as W
+    wl = W.generate(args.workload)
+    cfg = wl.cfg
+    pr = oracle.Problem(wl.q, wl.k_pool, wl.v_pool, wl.page_table, wl.seq_lens)
+    reps = oracle.build_reps(pr, wl.page_fill)
+    units = [(b, h) for b in range(cfg.batch) for h in range(cfg.kv_heads)]
+    t0 = time.perf_counter()
+    oracle.decode(pr, reps, cfg.draws, 0, *units[0])
+    t_unit = time.perf_counter() - t0
+    budget = 120.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    n_units = int(min(len(units), max(1, per_step // max(t_unit, 1e-9))))
+    steps = args.steps
+    note = ""
+    if n_units * t_unit * (steps + args.warmup) > 2 * budget:     # even one unit is too slow
+        steps = max(1, int(budget / t_unit) - args.warmup)
+        note = f"; {args.steps} steps asked, {steps} fit the time budget"
+    sample_units = units[:n_units]
+    for s_ in range(args.warmup):
+        for b, h in sample_units:
+            oracle.decode(pr, reps, cfg.draws, s_, b, h)
+    t0 = time.perf_counter()
+    for s_ in range(steps):
+        for b, h in sample_units:
+            oracle.decode(pr, reps, cfg.draws, args.warmup + s_, b, h)
+    el = (time.perf_counter() - t0) * len(units) / n_units
+    v = steps / el
+    sample = (f"{steps} steps, each decoding {n_units} of the {len(units)} (sequence, KV head) "
+              f"units; time scaled to whole steps{note}")
+    print(json.dumps({
+        "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
+                   "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "seq_len": cfg.seq_len,
+                   "team_size": cfg.team_size, "draws": cfg.draws},
+        "cpu_baseline": {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import sampled_sparse_decode_gb300 as santa
+    from sampled_sparse_decode_gb300 import binding as Bn
+    from sampled_sparse_decode_gb300 import workloads as W
+    import ctypes
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    wl = W.generate(args.workload)
+    cfg = wl.cfg
+    lib = Bn.lib()
+    esize = 2 if cfg.dtype == "bf16" else 4
+    units = cfg.batch * cfg.kv_heads
+    G, d, T, M = cfg.group, cfg.head_dim, cfg.team_size, cfg.draws
+    n_teams = wl.max_teams
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    q, k0, v0 = t(wl.q), t(wl.k_pool), t(wl.v_pool)
+    pt, lens, fill = t(wl.page_table), t(wl.seq_lens), t(wl.page_fill)
+    reps0 = santa.santa_build_reps(k0, fill)
+
+    # rotation: bytes touched per step (upper bound, |S| = M) x R >= 6 x L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    touched = units * (n_teams * d * 4 + min(M, n_teams) * T * 2 * d * esize)
+    pool_bytes = 2 * k0.numel() * esize + reps0.numel() * 4
+    free, _ = torch.cuda.mem_get_info(dev)
+    R = max(2, math.ceil(6 * l2 / touched))
+    R = min(R, max(2, int(0.4 * free // pool_bytes)))
+    ks = [k0] + [k0.clone() for _ in range(R - 1)]
+    vs = [v0] + [v0.clone() for _ in range(R - 1)]
+    reps = [reps0] + [reps0.clone() for _ in range(R - 1)]
+    bufs = Bn.DecodeBuffers.allocate(cfg.batch, cfg.q_heads, cfg.kv_heads, d, T, n_teams, M, dev)
+    dbufs = Bn.DecodeBuffers.allocate(cfg.batch, cfg.q_heads, cfg.kv_heads, d, T, n_teams, M,
+                                      dev, dense=True)
+    args_r = [Bn._args(q, ks[r], vs[r], reps[r], pt, lens, M, r, bufs) for r in range(R)]
+    dargs_r = [Bn._args(q, ks[r], vs[r], None, pt, lens, 1, 0, dbufs) for r in range(R)]
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    def call(fn, a):
+        rc = fn(ctypes.byref(a), sh)
+        if rc:
+            raise RuntimeError(f"{fn.__name__}: status {rc}")
+
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            body()                                   # warm (attribute set-up, lazy loading)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                body()
+        return g
+
+    def rounds(fn, arg_list):
+        """Graph maker for n steps of `fn` over the rotations (n <= R)."""
+        def make(nsteps):
+            return capture(lambda: [call(fn, arg_list[r]) for r in range(nsteps)])
+        return make
+
+    def timed(make, K, W_):
+        """Exactly K steps: K // R replays of an R-step graph and one (K mod R)-step tail."""
+        full, tail = K // R, K % R
+        g_full = make(R)
+        g_tail = make(tail) if tail else None
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, math.ceil(W_ / R))):
+                g_full.replay()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(full):
+                g_full.replay()
+            if g_tail is not None:
+                g_tail.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        barrier()
+        return e0.elapsed_time(e1) / 1e3, K, (t0, t1)
+
+    K, W_ = args.steps, max(3, args.warmup)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+
+    # ---- headline: whole decode steps
+    sec, steps_done, (c0, c1) = timed(rounds(lib.santa_decode, args_r), K, W_)
+    if world > 1:
+        tt = torch.tensor([sec], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        sec = float(tt.item())
+    step_s = sec / steps_done
+    value = world * steps_done / sec
+
+    # realised |S| of the R seeds (the graph replays them)
+    sel_total = 0
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            call(lib.santa_sample, args_r[r])
+            stream.synchronize()
+            sel_total += int(bufs.sel_count.sum().item())
+    mean_sel = sel_total / (R * units)
+    assert int(bufs.device_status.item()) == 0
+
+    # ---- the attention kernel alone (sampled sets of the last seed)
+    sec_a, n_a, _ = timed(rounds(lib.santa_attend, args_r), K, W_)
+    att_s = sec_a / n_a
+    with torch.cuda.stream(stream):
+        call(lib.santa_sample, args_r[R - 1])
+        stream.synchronize()
+    sel_last = int(bufs.sel_count.sum().item())
+    # attention-kernel algorithmic bytes: K and V of the sampled teams (valid tokens), q, out
+    att_bytes = sel_last * T * 2 * d * esize + cfg.batch * cfg.q_heads * d * (esize + 4)
+    # the sampling kernel alone (for the launch breakdown)
+    sec_s, n_s, _ = timed(rounds(lib.santa_sample, args_r), K, W_)
+    smp_s = sec_s / n_s
+
+    # ---- dense split-K reference on the same buffers
+    sec_d, n_d, _ = timed(rounds(lib.santa_dense_decode, dargs_r), max(R, K // 4), W_)
+    dense_s = sec_d / n_d
+    clocks.stop()
+    clk = clocks.summary(c0, c1)
+
+    # ---- bytes per step (realised |S|): reps of every team, K/V of the sampled teams, q, out
+    step_bytes = (units * n_teams * d * 4 + mean_sel * units * T * 2 * d * esize +
+                  cfg.batch * cfg.q_heads * d * (esize + 4))
+    dense_kv = units * cfg.seq_len * 2 * d * esize
+    peak, peak_kind = measured_peak()
+    achieved = att_bytes / att_s / 1e9
+
+    # ---- end to end through the Python API, host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = dict(pin_memory=True)
+        hq = q.cpu().clone().pin_memory()
+        hpt, hlens = pt.cpu().clone().pin_memory(), lens.cpu().clone().pin_memory()
+        hout = torch.empty(bufs.out.shape, dtype=torch.float32, **pin)
+        hsel = torch.empty(bufs.sel_ids.shape, dtype=torch.int32, **pin)
+        hdraw = torch.empty(bufs.draw_ids.shape, dtype=torch.int32, **pin)
+        hcnt = torch.empty(bufs.sel_count.shape, dtype=torch.int32, **pin)
+        hpi = torch.empty(bufs.pi.shape, dtype=torch.float32, **pin)
+        dq, dpt, dlens = torch.empty_like(q), torch.empty_like(pt), torch.empty_like(lens)
+        h2d = hq.numel() * hq.element_size() + hpt.numel() * 4 + hlens.numel() * 4
+        d2h = sum(x.numel() * x.element_size() for x in (hout, hsel, hdraw, hcnt, hpi))
+        K_e = max(20, min(K, 2000))
+
+        def e2e_step(s):
+            r = s % R
+            with torch.cuda.stream(stream):
+                dq.copy_(hq, non_blocking=True)
+                dpt.copy_(hpt, non_blocking=True)
+                dlens.copy_(hlens, non_blocking=True)
+                santa.santa_decode(dq, ks[r], vs[r], reps[r], dpt, dlens, M, s, bufs=bufs,
+                                   stream=stream)
+                hout.copy_(bufs.out, non_blocking=True)
+                hsel.copy_(bufs.sel_ids, non_blocking=True)
+                hdraw.copy_(bufs.draw_ids, non_blocking=True)
+                hcnt.copy_(bufs.sel_count, non_blocking=True)
+                hpi.copy_(bufs.pi, non_blocking=True)
+            stream.synchronize()
+
+        for s in range(W_):
+            e2e_step(s)
+        barrier()
+        t0 = time.perf_counter()
+        for s in range(K_e):
+            e2e_step(W_ + s)
+        el = time.perf_counter() - t0
+        if world > 1:
+            tt = torch.tensor([el], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            el = float(tt.item())
+        e2e = {"value": world * K_e / el, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": K_e}
+
+    # ---- CPU baseline (rank 0, single GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, el = oracle_steps_per_s(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} whole decode steps ({units} units each) in {el:.1f} s, "
+                         f"fp64 C oracle, one thread, reps precomputed"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": steps_done, "warmup": W_, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
+                   "kv_heads": cfg.kv_heads, "head_dim": d, "seq_len": cfg.seq_len,
+                   "team_size": T, "draws": M, "parallelism": "replicas" if world > 1 else "1gpu",
+                   "l2": f"inputs rotate over {R} copies of K/V/reps; touched bytes between "
+                         f"reuses of a copy >= 6x L2 at |S| = M ({l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graph of R steps replayed, CUDA events on the stream"},
+        "step_latency_us": step_s * 1e6,
+        "hbm_gbs_step": step_bytes / step_s / 1e9,
+        "bytes_per_step": step_bytes,
+        "kv_read_ratio": mean_sel * units * T * 2 * d * esize / dense_kv,
+        "mean_sel": mean_sel,
+        "dense": {"steps_per_s": 1.0 / dense_s, "latency_us": dense_s * 1e6,
+                  "hbm_gbs": dense_kv / dense_s / 1e9},
+        "speedup_vs_dense": dense_s / step_s,
+        "kernels_us": {"score_sample": smp_s * 1e6, "attend": att_s * 1e6,
+                       "dense_attend": dense_s * 1e6},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "attend_kernel (split-K Horvitz-Thompson attention)",
+                     "bytes_per_launch": att_bytes,
+                     "traffic": recorded_traffic(cfg.name)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * steps_done,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

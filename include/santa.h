@@ -78,6 +78,7 @@ typedef enum santa_dtype { SANTA_F32 = 0, SANTA_BF16 = 1 } santa_dtype;
 #define SANTA_DEV_BAD_PAGE 1u    /* a page id outside [0, num_pages) */
 #define SANTA_DEV_BAD_SEQLEN 2u  /* seq_len < 1 or seq_len > max_teams * team_size */
 #define SANTA_DEV_BAD_SEL 4u     /* santa_attend given a sel_ids/sel_count/pi entry out of range */
+#define SANTA_DEV_TIMEOUT 8u     /* a bounded wait on an asynchronous copy gave up (2 s) */
 
 /* Returns SANTA_ABI_VERSION of the loaded library. */
 int santa_abi_version(void);

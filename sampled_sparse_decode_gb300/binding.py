@@ -1,0 +1,281 @@
+"""Thin ctypes binding of libsanta.so: argument marshalling only.
+
+Every function takes torch CUDA tensors, checks their dtypes/shapes/layout, fills the C
+structure declared in include/santa.h and calls the entry point of the same name on the
+current torch stream.  All computation happens in the library's kernels; if the library
+cannot be loaded, the first call raises (there is no CPU fallback).
+
+Shapes (as in the C header): q [B][Hq][d]; k_pool, v_pool [P][Hkv][T][d] (float32 or
+bfloat16); reps [P][Hkv][d] float32; page_table [B][max_teams] int32; seq_lens [B] int32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+DEV_BAD_PAGE, DEV_BAD_SEQLEN, DEV_BAD_SEL, DEV_TIMEOUT = 1, 2, 4, 8
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+class SantaError(RuntimeError):
+    pass
+
+
+class _DecodeArgs(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+        ("reps", ctypes.c_void_p), ("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("dtype", ctypes.c_int), ("batch", ctypes.c_int), ("num_q_heads", ctypes.c_int),
+        ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("team_size", ctypes.c_int),
+        ("max_teams", ctypes.c_int), ("num_draws", ctypes.c_int),
+        ("num_pages", ctypes.c_int64), ("seed", ctypes.c_uint64),
+        ("out", ctypes.c_void_p), ("draw_ids", ctypes.c_void_p), ("sel_ids", ctypes.c_void_p),
+        ("sel_count", ctypes.c_void_p), ("pi", ctypes.c_void_p), ("team_probs", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("device_status", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """Load libsanta.so (building it from source first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        A = ctypes.POINTER(_DecodeArgs)
+        sigs = {
+            "santa_abi_version": (i32, []),
+            "santa_status_string": (ctypes.c_char_p, [i32]),
+            "santa_build_reps": (i32, [vp, i32, i64, i32, i32, i32, vp, vp, vp, vp]),
+            "santa_update_reps": (i32, [vp, i32, i64, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
+            "santa_decode_workspace_bytes": (sz, [i32] * 7),
+            "santa_decode_workspace_min_bytes": (sz, [i32] * 4),
+            "santa_dense_workspace_bytes": (sz, [i32] * 6),
+            "santa_sample": (i32, [A, vp]),
+            "santa_attend": (i32, [A, vp]),
+            "santa_decode": (i32, [A, vp]),
+            "santa_dense_decode": (i32, [A, vp]),
+        }
+        for name, (res, args) in sigs.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def santa_abi_version() -> int:
+    return lib().santa_abi_version()
+
+
+def santa_status_string(status: int) -> str:
+    return lib().santa_status_string(status).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise SantaError(f"{what}: {santa_status_string(rc)} (status {rc})")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _req(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise SantaError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise SantaError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise SantaError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise SantaError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t
+
+
+def santa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, team_size,
+                                 max_teams, num_draws) -> int:
+    return lib().santa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                              team_size, max_teams, num_draws)
+
+
+def santa_decode_workspace_min_bytes(batch, num_q_heads, num_kv_heads, head_dim) -> int:
+    return lib().santa_decode_workspace_min_bytes(batch, num_q_heads, num_kv_heads, head_dim)
+
+
+def santa_dense_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, team_size,
+                                max_teams) -> int:
+    return lib().santa_dense_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                             team_size, max_teams)
+
+
+def santa_build_reps(k_pool: torch.Tensor, page_fill: torch.Tensor | None = None,
+                     reps: torch.Tensor | None = None, device_status: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """Mean key of every (page, KV head) -> reps [P][Hkv][d] float32."""
+    _req(k_pool, "k_pool", ndim=4)
+    P, Hkv, T, d = k_pool.shape
+    if k_pool.dtype not in _DTYPES:
+        raise SantaError("k_pool must be float32 or bfloat16")
+    if reps is None:
+        reps = torch.empty((P, Hkv, d), dtype=torch.float32, device=k_pool.device)
+    _req(reps, "reps", torch.float32)
+    if page_fill is not None:
+        _req(page_fill, "page_fill", torch.int32)
+    _check(lib().santa_build_reps(_ptr(k_pool), _DTYPES[k_pool.dtype], P, Hkv, T, d,
+                                  _ptr(page_fill), _ptr(reps), _ptr(device_status),
+                                  _stream(stream)), "santa_build_reps")
+    return reps
+
+
+def santa_update_reps(k_pool: torch.Tensor, pages: torch.Tensor, reps: torch.Tensor,
+                      page_fill: torch.Tensor | None = None,
+                      device_status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Recompute the representatives of the listed pages in place."""
+    _req(k_pool, "k_pool", ndim=4)
+    _req(pages, "pages", torch.int32, 1)
+    _req(reps, "reps", torch.float32)
+    P, Hkv, T, d = k_pool.shape
+    _check(lib().santa_update_reps(_ptr(k_pool), _DTYPES[k_pool.dtype], P, Hkv, T, d,
+                                   _ptr(pages), pages.numel(), _ptr(page_fill), _ptr(reps),
+                                   _ptr(device_status), _stream(stream)), "santa_update_reps")
+    return reps
+
+
+@dataclass
+class DecodeBuffers:
+    """Outputs and scratch of one decode step for a fixed shape (reusable across steps)."""
+    out: torch.Tensor          # [B][Hq][d] float32
+    draw_ids: torch.Tensor     # [B][Hkv][M] int32
+    sel_ids: torch.Tensor      # [B][Hkv][M] int32
+    sel_count: torch.Tensor    # [B][Hkv] int32
+    pi: torch.Tensor           # [B][Hkv][M] float32
+    team_probs: torch.Tensor | None   # [B][Hkv][max_teams] float32
+    workspace: torch.Tensor    # uint8
+    device_status: torch.Tensor  # [1] int32
+
+    @staticmethod
+    def allocate(batch, num_q_heads, num_kv_heads, head_dim, team_size, max_teams, num_draws,
+                 device="cuda", team_probs=False, dense=False) -> "DecodeBuffers":
+        B, Hkv, M = batch, num_kv_heads, max(num_draws, 1)
+        ws = (santa_dense_workspace_bytes(B, num_q_heads, Hkv, head_dim, team_size, max_teams)
+              if dense else
+              santa_decode_workspace_bytes(B, num_q_heads, Hkv, head_dim, team_size, max_teams,
+                                           M))
+        if ws == 0:
+            raise SantaError("unsupported shape for the workspace query")
+        i32 = dict(dtype=torch.int32, device=device)
+        return DecodeBuffers(
+            out=torch.empty((B, num_q_heads, head_dim), dtype=torch.float32, device=device),
+            draw_ids=torch.empty((B, Hkv, M), **i32),
+            sel_ids=torch.empty((B, Hkv, M), **i32),
+            sel_count=torch.empty((B, Hkv), **i32),
+            pi=torch.empty((B, Hkv, M), dtype=torch.float32, device=device),
+            team_probs=(torch.empty((B, Hkv, max_teams), dtype=torch.float32, device=device)
+                        if team_probs else None),
+            workspace=torch.zeros(ws, dtype=torch.uint8, device=device),
+            device_status=torch.zeros(1, **i32),
+        )
+
+    def status(self) -> int:
+        """Synchronise with the device and return the device status word."""
+        return int(self.device_status.item())
+
+
+def _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed,
+          bufs: DecodeBuffers) -> _DecodeArgs:
+    _req(q, "q", ndim=3)
+    _req(k_pool, "k_pool", ndim=4)
+    _req(v_pool, "v_pool", ndim=4)
+    _req(page_table, "page_table", torch.int32, 2)
+    _req(seq_lens, "seq_lens", torch.int32, 1)
+    if q.dtype not in _DTYPES or k_pool.dtype != q.dtype or v_pool.dtype != q.dtype:
+        raise SantaError("q, k_pool and v_pool must share one dtype (float32 or bfloat16)")
+    if k_pool.shape != v_pool.shape:
+        raise SantaError("k_pool and v_pool must have the same shape")
+    if reps is not None:
+        _req(reps, "reps", torch.float32, 3)
+    B, Hq, d = q.shape
+    P, Hkv, T, d2 = k_pool.shape
+    if d2 != d or page_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise SantaError("shape mismatch between q, k_pool, page_table and seq_lens")
+    a = _DecodeArgs()
+    a.q, a.k_pool, a.v_pool, a.reps = _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(reps)
+    a.page_table, a.seq_lens = _ptr(page_table), _ptr(seq_lens)
+    a.dtype, a.batch, a.num_q_heads, a.num_kv_heads = _DTYPES[q.dtype], B, Hq, Hkv
+    a.head_dim, a.team_size, a.max_teams, a.num_draws = d, T, page_table.shape[1], num_draws
+    a.num_pages, a.seed = P, seed & 0xFFFFFFFFFFFFFFFF
+    a.out, a.draw_ids, a.sel_ids = _ptr(bufs.out), _ptr(bufs.draw_ids), _ptr(bufs.sel_ids)
+    a.sel_count, a.pi, a.team_probs = _ptr(bufs.sel_count), _ptr(bufs.pi), _ptr(bufs.team_probs)
+    a.workspace, a.workspace_bytes = _ptr(bufs.workspace), bufs.workspace.numel()
+    a.device_status = _ptr(bufs.device_status)
+    return a
+
+
+def _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs=False, dense=False):
+    if bufs is not None:
+        return bufs
+    B, Hq, d = q.shape
+    _, Hkv, T, _ = k_pool.shape
+    return DecodeBuffers.allocate(B, Hq, Hkv, d, T, page_table.shape[1], num_draws, q.device,
+                                  team_probs=team_probs, dense=dense)
+
+
+def santa_sample(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, seed: int,
+                 bufs: DecodeBuffers | None = None, team_probs: bool = False,
+                 stream=None) -> DecodeBuffers:
+    """Team distribution, M draws, distinct set and inclusion probabilities."""
+    bufs = _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs)
+    a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs)
+    _check(lib().santa_sample(ctypes.byref(a), _stream(stream)), "santa_sample")
+    return bufs
+
+
+def santa_attend(q, k_pool, v_pool, page_table, seq_lens, sel_ids, sel_count, pi,
+                 bufs: DecodeBuffers | None = None, stream=None) -> DecodeBuffers:
+    """Horvitz-Thompson attention over the given teams (sel_ids [B][Hkv][M], sel_count
+    [B][Hkv], pi [B][Hkv][M]); writes bufs.out."""
+    _req(sel_ids, "sel_ids", torch.int32, 3)
+    _req(sel_count, "sel_count", torch.int32, 2)
+    _req(pi, "pi", torch.float32, 3)
+    M = sel_ids.shape[2]
+    bufs = _bufs_for(q, k_pool, page_table, M, bufs)
+    a = _args(q, k_pool, v_pool, None, page_table, seq_lens, M, 0, bufs)
+    a.sel_ids, a.sel_count, a.pi = _ptr(sel_ids), _ptr(sel_count), _ptr(pi)
+    _check(lib().santa_attend(ctypes.byref(a), _stream(stream)), "santa_attend")
+    return bufs
+
+
+def santa_decode(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, seed: int,
+                 bufs: DecodeBuffers | None = None, team_probs: bool = False,
+                 stream=None) -> DecodeBuffers:
+    """One SANTA++ decode step: sampling then Horvitz-Thompson attention."""
+    bufs = _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs)
+    a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs)
+    _check(lib().santa_decode(ctypes.byref(a), _stream(stream)), "santa_decode")
+    return bufs
+
+
+def santa_dense_decode(q, k_pool, v_pool, page_table, seq_lens,
+                       bufs: DecodeBuffers | None = None, stream=None) -> DecodeBuffers:
+    """Exact dense split-K decode attention over every token (the speed reference)."""
+    bufs = _bufs_for(q, k_pool, page_table, 1, bufs, dense=True)
+    a = _args(q, k_pool, v_pool, None, page_table, seq_lens, 1, 0, bufs)
+    _check(lib().santa_dense_decode(ctypes.byref(a), _stream(stream)), "santa_dense_decode")
+    return bufs

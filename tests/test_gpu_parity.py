@@ -1,0 +1,228 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Rules: sampled team ids bit-exact, except draws whose oracle u*Z lies within 1e-6 of an
+oracle CDF value (counted, < 1e-4 of draws); inclusion probabilities within 1e-5 relative;
+outputs computed on identical sampled sets (the oracle's) within 1e-5 max-abs for fp32
+inputs and 2e-3 for bf16 inputs; representatives and dense attention likewise.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sampled_sparse_decode_gb300 as santa
+from sampled_sparse_decode_gb300 import workloads as W
+from helpers import (BOUNDARY_SHARE, TOL_OUT, TOL_PI, DeviceWorkload, compare_draws,
+                     full_oracle_reps, full_workload, problem)
+
+pytestmark = pytest.mark.gpu
+
+NAN = float("nan")
+
+# Reduced-size variants of every workload: the same distributions, several tiles per unit,
+# ragged sequence ends (NaN in the unused page slots) and mixed lengths in one batch.
+SMALL = {
+    "tiny_f32": dict(cfg="tiny_f32"),
+    "qwen_b2_ragged": dict(cfg="qwen7b_32k_b1_m31", batch=2, seq_len=4000),
+    "qwen_b3_mixed_m64": dict(cfg="qwen7b_32k_b8_m64", batch=3, seq_lens=[4096, 3000, 129]),
+    "llama_paged_b4": dict(cfg="llama8b_paged_32k_b16_m32", batch=4, seq_len=6000,
+                           num_pages=300),
+    "long_paged_b2": dict(cfg="long_128k_b4_m64", batch=2, seq_len=20000, num_pages=0),
+    "bf16_d64_t64": dict(cfg="qwen7b_32k_b1_m31", head_dim=64, team_size=64, seq_len=3000,
+                         q_heads=8, kv_heads=2, draws=20),
+    "f32_d128_g8": dict(cfg="tiny_f32", head_dim=128, team_size=128, seq_len=5000,
+                        q_heads=16, kv_heads=2, draws=12),
+}
+
+
+def make(spec, **extra):
+    spec = dict(spec, **extra)
+    name = spec.pop("cfg")
+    seq_lens = spec.pop("seq_lens", None)
+    if seq_lens is not None:
+        spec["batch"] = len(seq_lens)
+    return W.generate(name, seq_lens=seq_lens, invalid_fill=NAN, **spec)
+
+
+def run_sample(dw: DeviceWorkload, reps, M, seed):
+    bufs = santa.santa_sample(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
+                              M, seed, team_probs=True)
+    torch.cuda.synchronize()
+    return bufs
+
+
+def check_unit_sampling(wl, pr, reps_o, bufs, M, seed, b, h):
+    """Compares one unit's p, draws, S and pi with the oracle; returns draw statistics."""
+    p = oracle.team_probs(pr, reps_o, b, h)
+    n = p.size
+    p_gpu = bufs.team_probs[b, h, :n].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(p_gpu, p, rtol=1e-5, atol=1e-7 * p.max())
+    assert (bufs.team_probs[b, h, n:].cpu().numpy() == 0).all()
+    draws, t, C = oracle.draw(p, M, seed, b, h)
+    g_draws = bufs.draw_ids[b, h].cpu().numpy()
+    inside, outside = compare_draws(g_draws, draws, t, C)
+    assert outside == 0, f"unit ({b},{h}): {outside} draws differ away from any CDF boundary"
+    cnt = int(bufs.sel_count[b, h])
+    sel = bufs.sel_ids[b, h].cpu().numpy()
+    pi = bufs.pi[b, h].cpu().numpy()
+    # S is the ascending distinct set of the GPU's own draws, padded with -1 / 0
+    assert np.array_equal(sel[:cnt], np.unique(g_draws))
+    assert (sel[cnt:] == -1).all() and (pi[cnt:] == 0).all()
+    if inside == 0:
+        o_sel, o_pi = oracle.select(draws, p)
+        assert np.array_equal(sel[:cnt], o_sel)
+        np.testing.assert_allclose(pi[:cnt], o_pi, rtol=TOL_PI)
+    return inside, M
+
+
+def check_unit_attend(wl, pr, dw, b, h, o_sel, o_pi, out_gpu, tol):
+    want = oracle.attend(pr, b, h, o_sel, o_pi)
+    G = wl.cfg.group
+    got = out_gpu[b, h * G:(h + 1) * G].cpu().numpy().astype(np.float64)
+    err = np.abs(got - want).max()
+    assert err <= tol, f"unit ({b},{h}): max-abs error {err:.3g} > {tol}"
+    return err
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_reps_parity(name):
+    wl = make(SMALL[name])
+    dw = DeviceWorkload(wl)
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    torch.cuda.synchronize()
+    want = oracle.build_reps(problem(wl), wl.page_fill)
+    got = reps.cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(got, want, rtol=1e-5, atol=1e-6 * np.abs(want).max())
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_sample_and_attend_parity(name):
+    wl = make(SMALL[name])
+    cfg = wl.cfg
+    dw = DeviceWorkload(wl)
+    pr = problem(wl)
+    reps_o = oracle.build_reps(pr, wl.page_fill)
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    seed = 1234
+    bufs = run_sample(dw, reps, cfg.draws, seed)
+    inside = total = 0
+    sels, pis, units = [], [], []
+    for b in range(cfg.batch):
+        for h in range(cfg.kv_heads):
+            i, m = check_unit_sampling(wl, pr, reps_o, bufs, cfg.draws, seed, b, h)
+            inside, total = inside + i, total + m
+            p = oracle.team_probs(pr, reps_o, b, h)
+            d, _, _ = oracle.draw(p, cfg.draws, seed, b, h)
+            s, pi = oracle.select(d, p)
+            units.append((b, h))
+            sels.append(s)
+            pis.append(pi)
+    assert inside <= BOUNDARY_SHARE * total
+    # attention on the oracle's sampled sets and inclusion probabilities
+    M = cfg.draws
+    sel_t = torch.full((cfg.batch, cfg.kv_heads, M), -1, dtype=torch.int32)
+    cnt_t = torch.zeros((cfg.batch, cfg.kv_heads), dtype=torch.int32)
+    pi_t = torch.zeros((cfg.batch, cfg.kv_heads, M), dtype=torch.float32)
+    for (b, h), s, pi in zip(units, sels, pis):
+        sel_t[b, h, :s.size] = torch.from_numpy(s)
+        cnt_t[b, h] = s.size
+        pi_t[b, h, :s.size] = torch.from_numpy(pi.astype(np.float32))
+    ab = santa.santa_attend(dw.q, dw.k_pool, dw.v_pool, dw.page_table, dw.seq_lens,
+                            sel_t.cuda(), cnt_t.cuda(), pi_t.cuda())
+    torch.cuda.synchronize()
+    assert ab.status() == 0
+    tol = TOL_OUT[cfg.dtype]
+    for (b, h), s, pi in zip(units, sels, pis):
+        check_unit_attend(wl, pr, dw, b, h, s, pi, ab.out, tol)
+    # the whole step in one call: same sets wherever the draws agreed
+    db = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens, M,
+                            seed)
+    torch.cuda.synchronize()
+    assert db.status() == 0
+    for (b, h), s, pi in zip(units, sels, pis):
+        if int(db.sel_count[b, h]) == s.size and np.array_equal(
+                db.sel_ids[b, h, :s.size].cpu().numpy(), s):
+            check_unit_attend(wl, pr, dw, b, h, s, pi, db.out, tol)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_dense_parity(name):
+    wl = make(SMALL[name])
+    dw = DeviceWorkload(wl)
+    pr = problem(wl)
+    bufs = santa.santa_dense_decode(dw.q, dw.k_pool, dw.v_pool, dw.page_table, dw.seq_lens)
+    torch.cuda.synchronize()
+    assert bufs.status() == 0
+    G, tol = wl.cfg.group, TOL_OUT[wl.cfg.dtype]
+    for b in range(wl.cfg.batch):
+        for h in range(wl.cfg.kv_heads):
+            want = oracle.dense(pr, b, h)
+            got = bufs.out[b, h * G:(h + 1) * G].cpu().numpy()
+            assert np.abs(got - want).max() <= tol
+
+
+def test_seed_sweep_draws_bit_exact():
+    """4096 decode seeds of the tiny fp32 workload: every draw equals the oracle's, except
+    draws inside the CDF-boundary window, which stay below 1e-4 of all draws."""
+    wl = W.generate("tiny_f32")
+    dw = DeviceWorkload(wl)
+    pr = problem(wl)
+    reps_o = oracle.build_reps(pr)
+    reps = santa.santa_build_reps(dw.k_pool)
+    p = oracle.team_probs(pr, reps_o, 0, 0)
+    M = wl.cfg.draws
+    bufs = None
+    seeds = range(4096)
+    gpu = torch.empty((len(seeds), M), dtype=torch.int32, device="cuda")
+    for k, seed in enumerate(seeds):
+        bufs = santa.santa_sample(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
+                                  M, seed, bufs=bufs)
+        gpu[k].copy_(bufs.draw_ids[0, 0])
+    gpu = gpu.cpu().numpy()
+    inside = 0
+    for k, seed in enumerate(seeds):
+        draws, t, C = oracle.draw(p, M, seed, 0, 0)
+        i, o = compare_draws(gpu[k], draws, t, C)
+        assert o == 0, f"seed {seed}: draws differ away from a CDF boundary"
+        inside += i
+    assert inside < BOUNDARY_SHARE * gpu.size
+
+
+FULL = ["qwen7b_32k_b1_m31", "qwen7b_32k_b8_m64", "llama8b_paged_32k_b16_m32", "long_128k_b4_m64"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_units(name):
+    """Full-size workloads in the launch configuration the benchmark times (santa_decode with
+    the default workspace); the oracle checks a sample of units one by one."""
+    wl = full_workload(name)
+    cfg = wl.cfg
+    dw = DeviceWorkload(wl)
+    pr = problem(wl)
+    reps_o = full_oracle_reps(name)
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    seed = 7
+    bufs = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
+                              cfg.draws, seed, team_probs=True)
+    torch.cuda.synchronize()
+    assert bufs.status() == 0
+    units = sorted({(0, 0), (cfg.batch // 2, cfg.kv_heads // 2),
+                    (cfg.batch - 1, cfg.kv_heads - 1)})
+    tol = TOL_OUT[cfg.dtype]
+    for b, h in units:
+        check_unit_sampling(wl, pr, reps_o, bufs, cfg.draws, seed, b, h)
+        p = oracle.team_probs(pr, reps_o, b, h)
+        d, _, _ = oracle.draw(p, cfg.draws, seed, b, h)
+        s, pi = oracle.select(d, p)
+        if np.array_equal(bufs.sel_ids[b, h, :s.size].cpu().numpy(), s):
+            check_unit_attend(wl, pr, dw, b, h, s, pi, bufs.out, tol)
+    # properties that hold for every unit at any size
+    cnt = bufs.sel_count.cpu().numpy()
+    assert (cnt >= 1).all() and (cnt <= min(cfg.draws, cfg.n_teams)).all()
+    assert torch.isfinite(bufs.out).all()
+    pi = bufs.pi.cpu().numpy()
+    for b in range(cfg.batch):
+        for h in range(cfg.kv_heads):
+            assert (pi[b, h, :cnt[b, h]] > 0).all() and (pi[b, h, :cnt[b, h]] <= 1).all()
