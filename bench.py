@@ -56,6 +56,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
+                    help="profile: W + K plain santa_decode (or --dense) steps on one copy of "
+                         "the inputs, for ncu captures")
+    ap.add_argument("--dense", action="store_true", help="profile mode: the dense kernel")
     return ap.parse_args()
 
 
@@ -275,9 +279,10 @@ def run_ours(args):
     ks = [k0] + [k0.clone() for _ in range(R - 1)]
     vs = [v0] + [v0.clone() for _ in range(R - 1)]
     reps = [reps0] + [reps0.clone() for _ in range(R - 1)]
-    bufs = Bn.DecodeBuffers.allocate(cfg.batch, cfg.q_heads, cfg.kv_heads, d, T, n_teams, M, dev)
-    dbufs = Bn.DecodeBuffers.allocate(cfg.batch, cfg.q_heads, cfg.kv_heads, d, T, n_teams, M,
-                                      dev, dense=True)
+    bufs = Bn.DecodeBuffers.allocate(q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads, d, T,
+                                     n_teams, M, dev)
+    dbufs = Bn.DecodeBuffers.allocate(q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads, d, T,
+                                      n_teams, M, dev, dense=True)
     args_r = [Bn._args(q, ks[r], vs[r], reps[r], pt, lens, M, r, bufs) for r in range(R)]
     dargs_r = [Bn._args(q, ks[r], vs[r], None, pt, lens, 1, 0, dbufs) for r in range(R)]
     stream = torch.cuda.Stream(device=dev)
@@ -466,9 +471,43 @@ def run_ours(args):
     print(json.dumps(line))
 
 
+def run_profile(args):
+    """A short run for ncu: one copy of the inputs, W + K steps launched on the stream."""
+    import numpy as np
+    import torch
+    import sampled_sparse_decode_gb300 as santa
+    from sampled_sparse_decode_gb300 import workloads as W
+    wl = W.generate(args.workload)
+    cfg = wl.cfg
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    q, k, v = t(wl.q), t(wl.k_pool), t(wl.v_pool)
+    pt, lens, fill = t(wl.page_table), t(wl.seq_lens), t(wl.page_fill)
+    reps = santa.santa_build_reps(k, fill)
+    bufs = None
+    for s_ in range(args.warmup + args.steps):
+        if args.dense:
+            bufs = santa.santa_dense_decode(q, k, v, pt, lens, bufs=bufs)
+        else:
+            bufs = santa.santa_decode(q, k, v, reps, pt, lens, cfg.draws, s_, bufs=bufs)
+    torch.cuda.synchronize()
+    st = bufs.status()
+    print(json.dumps({"mode": "profile", "workload": cfg.name, "dense": args.dense,
+                      "steps": args.warmup + args.steps, "device_status": st,
+                      "sel_count": None if args.dense else bufs.sel_count.sum().item()}))
+    if st:
+        raise SystemExit(1)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.mode == "profile":
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -148,14 +148,17 @@ typedef struct santa_decode_args {
 
 /*
  * Workspace for santa_attend / santa_decode: split-K partials (m, l, acc[d]) per query head
- * and one arrival counter per unit.  Returns the size the library's default split plan
- * uses on the current device; any smaller size of at least
- * santa_decode_workspace_min_bytes still works, with fewer, longer splits.
+ * and one arrival counter per unit.  santa_decode_workspace_bytes returns the size of the
+ * library's default split plan on the current device (one wave of resident attention CTAs;
+ * 0 for an unsupported shape); any size down to santa_decode_workspace_min_bytes also works,
+ * with fewer, longer splits.  The workspace of santa_dense_decode is sized the same way by
+ * santa_dense_workspace_bytes.  A workspace is used by one call at a time.
  */
-size_t santa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+size_t santa_decode_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
                                     int head_dim, int team_size, int max_teams, int num_draws);
 size_t santa_decode_workspace_min_bytes(int batch, int num_q_heads, int num_kv_heads,
-                                        int head_dim);
+                                        int head_dim, int team_size, int max_teams,
+                                        int num_draws);
 
 /*
  * santa_sample — score the representatives, form the GQA-mixed team distribution, draw M
@@ -188,7 +191,7 @@ int santa_decode(const santa_decode_args* a, void* stream);
  * page_table, seq_lens and the shape fields; writes out; uses workspace and device_status.
  * reps, num_draws, seed and the sampling outputs are ignored.
  */
-size_t santa_dense_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+size_t santa_dense_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
                                    int head_dim, int team_size, int max_teams);
 int santa_dense_decode(const santa_decode_args* a, void* stream);
 

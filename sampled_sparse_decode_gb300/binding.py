@@ -59,9 +59,9 @@ def lib():
             "santa_status_string": (ctypes.c_char_p, [i32]),
             "santa_build_reps": (i32, [vp, i32, i64, i32, i32, i32, vp, vp, vp, vp]),
             "santa_update_reps": (i32, [vp, i32, i64, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
-            "santa_decode_workspace_bytes": (sz, [i32] * 7),
-            "santa_decode_workspace_min_bytes": (sz, [i32] * 4),
-            "santa_dense_workspace_bytes": (sz, [i32] * 6),
+            "santa_decode_workspace_bytes": (sz, [i32] * 8),
+            "santa_decode_workspace_min_bytes": (sz, [i32] * 7),
+            "santa_dense_workspace_bytes": (sz, [i32] * 7),
             "santa_sample": (i32, [A, vp]),
             "santa_attend": (i32, [A, vp]),
             "santa_decode": (i32, [A, vp]),
@@ -109,20 +109,30 @@ def _req(t: torch.Tensor, name: str, dtype=None, ndim=None):
     return t
 
 
-def santa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, team_size,
+def _dtype_code(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    return _DTYPES[dtype]
+
+
+def santa_decode_workspace_bytes(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size,
                                  max_teams, num_draws) -> int:
-    return lib().santa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
-                                              team_size, max_teams, num_draws)
+    """dtype: torch.float32 / torch.bfloat16 (or 0 / 1)."""
+    return lib().santa_decode_workspace_bytes(_dtype_code(dtype), batch, num_q_heads,
+                                              num_kv_heads, head_dim, team_size, max_teams,
+                                              num_draws)
 
 
-def santa_decode_workspace_min_bytes(batch, num_q_heads, num_kv_heads, head_dim) -> int:
-    return lib().santa_decode_workspace_min_bytes(batch, num_q_heads, num_kv_heads, head_dim)
+def santa_decode_workspace_min_bytes(batch, num_q_heads, num_kv_heads, head_dim, team_size,
+                                     max_teams, num_draws) -> int:
+    return lib().santa_decode_workspace_min_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                  team_size, max_teams, num_draws)
 
 
-def santa_dense_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, team_size,
+def santa_dense_workspace_bytes(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size,
                                 max_teams) -> int:
-    return lib().santa_dense_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
-                                             team_size, max_teams)
+    return lib().santa_dense_workspace_bytes(_dtype_code(dtype), batch, num_q_heads,
+                                             num_kv_heads, head_dim, team_size, max_teams)
 
 
 def santa_build_reps(k_pool: torch.Tensor, page_fill: torch.Tensor | None = None,
@@ -171,13 +181,15 @@ class DecodeBuffers:
     device_status: torch.Tensor  # [1] int32
 
     @staticmethod
-    def allocate(batch, num_q_heads, num_kv_heads, head_dim, team_size, max_teams, num_draws,
-                 device="cuda", team_probs=False, dense=False) -> "DecodeBuffers":
+    def allocate(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size, max_teams,
+                 num_draws, device="cuda", team_probs=False, dense=False) -> "DecodeBuffers":
+        """dtype of q/K/V (torch.float32 or torch.bfloat16); sizes as in santa.h."""
         B, Hkv, M = batch, num_kv_heads, max(num_draws, 1)
-        ws = (santa_dense_workspace_bytes(B, num_q_heads, Hkv, head_dim, team_size, max_teams)
+        ws = (santa_dense_workspace_bytes(dtype, B, num_q_heads, Hkv, head_dim, team_size,
+                                          max_teams)
               if dense else
-              santa_decode_workspace_bytes(B, num_q_heads, Hkv, head_dim, team_size, max_teams,
-                                           M))
+              santa_decode_workspace_bytes(dtype, B, num_q_heads, Hkv, head_dim, team_size,
+                                           max_teams, M))
         if ws == 0:
             raise SantaError("unsupported shape for the workspace query")
         i32 = dict(dtype=torch.int32, device=device)
@@ -233,8 +245,8 @@ def _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs=False, dense=Fa
         return bufs
     B, Hq, d = q.shape
     _, Hkv, T, _ = k_pool.shape
-    return DecodeBuffers.allocate(B, Hq, Hkv, d, T, page_table.shape[1], num_draws, q.device,
-                                  team_probs=team_probs, dense=dense)
+    return DecodeBuffers.allocate(q.dtype, B, Hq, Hkv, d, T, page_table.shape[1], num_draws,
+                                  q.device, team_probs=team_probs, dense=dense)
 
 
 def santa_sample(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, seed: int,

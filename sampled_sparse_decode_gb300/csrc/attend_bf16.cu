@@ -14,4 +14,8 @@ size_t attend_smem_bytes_bf16(int head_dim, int group) {
   return head_dim == 128 ? attend_smem_g<true, 128>(group) : attend_smem_g<true, 64>(group);
 }
 
+int attend_resident_ctas_bf16(int head_dim, int group) {
+  return head_dim == 128 ? attend_resident_g<true, 128>(group) : attend_resident_g<true, 64>(group);
+}
+
 }  // namespace santa

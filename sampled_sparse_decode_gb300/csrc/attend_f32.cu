@@ -14,4 +14,8 @@ size_t attend_smem_bytes_f32(int head_dim, int group) {
   return head_dim == 128 ? attend_smem_g<false, 128>(group) : attend_smem_g<false, 64>(group);
 }
 
+int attend_resident_ctas_f32(int head_dim, int group) {
+  return head_dim == 128 ? attend_resident_g<false, 128>(group) : attend_resident_g<false, 64>(group);
+}
+
 }  // namespace santa

@@ -36,6 +36,14 @@
 
 namespace santa {
 
+// Where a staged chunk comes from and how it is weighted.
+struct ChunkMeta {
+  int page;      // physical page, or -1 for a chunk that contributes nothing
+  int valid;     // valid tokens in the chunk (0..64)
+  float lw2;     // -log2(pi) of its team (0 in dense mode)
+  int part;      // which 64-token half of the page
+};
+
 template <bool BF16, int D, int G>
 struct AttendTraits {
   static constexpr int kThreads = 256;
@@ -48,11 +56,15 @@ struct AttendTraits {
   static constexpr int kEplV = D / 32;                                // P.V-phase elements
   static constexpr int kMergeFloats = kWarps * G * D + 2 * kWarps * kMaxGroup;
   static_assert(kMergeFloats * 4 <= kStages * kStageBytes, "merge buffer must fit the stages");
-  // dynamic shared memory: stages | p rows [8][64] | alpha [8][8] | meta [stages] | bars
+  // two CTAs per SM when their stages fit (bf16, and fp32 with d = 64)
+  static constexpr int kMinBlocks = kStages * kStageBytes <= 100 * 1024 ? 2 : 1;
+  static constexpr int kCombineFloats = 3 * kMaxSplits * G + 2 * kMaxGroup;
+  static_assert(kCombineFloats * 4 <= kStages * kStageBytes, "combine scratch must fit");
+  // dynamic shared memory: stages | p rows [8][64] | alpha [8][8] | chunk table | bars
   static constexpr size_t kPOff = static_cast<size_t>(kStages) * kStageBytes;
   static constexpr size_t kAOff = kPOff + sizeof(float) * kWarps * 64;
   static constexpr size_t kMetaOff = kAOff + sizeof(float) * kWarps * kMaxGroup;
-  static constexpr size_t kBarOff = kMetaOff + sizeof(float2) * kStages;
+  static constexpr size_t kBarOff = kMetaOff + sizeof(ChunkMeta) * kMaxChunksPerSplit;
   static constexpr size_t kSmem = kBarOff + sizeof(uint64_t) * kStages;
 };
 
@@ -135,14 +147,15 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[8], int lane) 
 }
 
 template <bool BF16, int D, int G>
-__global__ void __launch_bounds__(256, 1) attend_kernel(const AttendParams p) {
+__global__ void __launch_bounds__(256, (AttendTraits<BF16, D, G>::kMinBlocks))
+    attend_kernel(const AttendParams p) {
   using Tr = AttendTraits<BF16, D, G>;
   constexpr int S = Tr::kStages;
   constexpr float kNegInf = -INFINITY;
   extern __shared__ __align__(128) unsigned char smem[];
-  float* prow = reinterpret_cast<float*>(smem + Tr::kPOff);      // [warp][token 8][head 8]
-  float* arow = reinterpret_cast<float*>(smem + Tr::kAOff);      // [warp][head 8]
-  float2* meta = reinterpret_cast<float2*>(smem + Tr::kMetaOff); // (valid tokens, -log2 pi)
+  float* prow = reinterpret_cast<float*>(smem + Tr::kPOff);        // [warp][token 8][head 8]
+  float* arow = reinterpret_cast<float*>(smem + Tr::kAOff);        // [warp][head 8]
+  ChunkMeta* meta = reinterpret_cast<ChunkMeta*>(smem + Tr::kMetaOff);  // [chunks of split]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Tr::kBarOff);
   __shared__ int s_last;
   __shared__ int s_abort;
@@ -172,7 +185,6 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(const AttendParams p) {
                                                              p.team_size;
   const int n = len_ok ? (L + p.team_size - 1) / p.team_size : 0;
   const int cpt = p.team_size / kChunk;                  // chunks per team
-  __syncthreads();
 
   pdl_wait();  // sel_ids / sel_count / pi / counters come from the sampling kernel
 
@@ -198,11 +210,9 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(const AttendParams p) {
   const int c_begin = split * p.chunks_per_split;
   const int n_chunks = min(c_begin + p.chunks_per_split, total_chunks) - c_begin;
 
-  const unsigned char* kpool = static_cast<const unsigned char*>(p.k_pool);
-  const unsigned char* vpool = static_cast<const unsigned char*>(p.v_pool);
-  // Producer: stage the c-th chunk of this split (thread 0 only).
-  auto issue = [&](int ci) {
-    const int c = c_begin + ci, stage = ci % S;
+  // ---- chunk table of this split, all chunks resolved in parallel
+  for (int ci = tid; ci < n_chunks; ci += Tr::kThreads) {
+    const int c = c_begin + ci;
     const int slot = c / cpt, part = c - slot * cpt;
     int team = slot;
     float lw2 = 0.f;
@@ -215,20 +225,31 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(const AttendParams p) {
       if (!ok) set_status(p.status, SANTA_DEV_BAD_SEL);
       lw2 = ok ? -log2f(piv) : 0.f;
     }
-    int64_t page = -1;
+    int page = -1;
     if (ok) {
       page = p.page_table[static_cast<int64_t>(b) * p.max_teams + team];
       if (page < 0 || page >= p.num_pages) {
         set_status(p.status, SANTA_DEV_BAD_PAGE);
         ok = false;
+        page = -1;
       }
     }
-    int vt = 0;
-    if (ok) vt = max(0, min(min(p.team_size, L - team * p.team_size) - part * kChunk, kChunk));
-    meta[stage] = make_float2(static_cast<float>(vt), lw2);
-    if (vt > 0) {
-      const int64_t off = ((page * p.num_kv_heads + h) * static_cast<int64_t>(p.team_size) +
-                           part * kChunk) * D * Tr::kEsize;
+    const int vt =
+        ok ? max(0, min(min(p.team_size, L - team * p.team_size) - part * kChunk, kChunk)) : 0;
+    meta[ci] = ChunkMeta{vt > 0 ? page : -1, vt, lw2, part};
+  }
+  __syncthreads();
+
+  const unsigned char* kpool = static_cast<const unsigned char*>(p.k_pool);
+  const unsigned char* vpool = static_cast<const unsigned char*>(p.v_pool);
+  // Producer: stage chunk ci of this split (one thread per call).
+  auto issue = [&](int ci) {
+    const int stage = ci % S;
+    const ChunkMeta m = meta[ci];
+    if (m.page >= 0) {
+      const int64_t off = ((static_cast<int64_t>(m.page) * p.num_kv_heads + h) *
+                               static_cast<int64_t>(p.team_size) + m.part * kChunk) *
+                          D * Tr::kEsize;
       unsigned char* dst = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
       mbar_arrive_expect_tx(&bar[stage], 2u * Tr::kChunkBytes);
       bulk_g2s(dst, kpool + off, Tr::kChunkBytes, &bar[stage]);
@@ -237,8 +258,7 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(const AttendParams p) {
       mbar_arrive(&bar[stage]);
     }
   };
-  if (tid == 0)
-    for (int ci = 0; ci < min(S, n_chunks); ++ci) issue(ci);
+  if (tid < min(S, n_chunks)) issue(tid);
 
   float m_run = kNegInf, l_run = 0.f;
   float acc[G][Tr::kEplV];
@@ -259,9 +279,8 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(const AttendParams p) {
     __syncthreads();
     if (s_abort) break;
     consumed = ci + 1;
-    const float2 mt = meta[stage];
-    const int vt = static_cast<int>(mt.x);
-    const float lw2 = mt.y;
+    const int vt = meta[ci].valid;
+    const float lw2 = meta[ci].lw2;
     const unsigned char* ks = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
     const unsigned char* vs = ks + Tr::kChunkBytes;
 
@@ -390,21 +409,77 @@ __global__ void __launch_bounds__(256, 1) attend_kernel(const AttendParams p) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int i = tid; i < G * D; i += Tr::kThreads) {
-    const int g = i / D, k = i - g * D;
+  float* cm_s = reinterpret_cast<float*>(smem);                     // [active][G] maxima
+  float* cl_s = cm_s + kMaxSplits * G;                              // [active][G] sums
+  float* cw_s = cl_s + kMaxSplits * G;                              // [active][G] weights
+  float* gm_s = cw_s + kMaxSplits * G;                              // [G] overall maxima
+  float* gl_s = gm_s + kMaxGroup;                                   // [G] overall sums
+  for (int i = tid; i < active * G; i += Tr::kThreads) {
+    cm_s[i] = __ldcg(&p.part_ml[(part_base * G + i) * 2]);
+    cl_s[i] = __ldcg(&p.part_ml[(part_base * G + i) * 2 + 1]);
+  }
+  __syncthreads();
+  if (warp < G) {
     float mx = kNegInf;
-    for (int c = 0; c < active; ++c)
-      mx = fmaxf(mx, __ldcg(&p.part_ml[((part_base + c) * G + g) * 2]));
-    float a = 0.f, l = 0.f;
+    for (int c = lane; c < active; c += 32) mx = fmaxf(mx, cm_s[c * G + warp]);
+    mx = warp_max(mx);
+    if (lane == 0) gm_s[warp] = mx;
+  }
+  __syncthreads();
+  for (int i = tid; i < active * G; i += Tr::kThreads) {
+    const float mc = cm_s[i];
+    cw_s[i] = mc == kNegInf ? 0.f : exp2f(mc - gm_s[i % G]);
+  }
+  __syncthreads();
+  if (warp < G) {
+    float l = 0.f;
+    for (int c = lane; c < active; c += 32) l = fmaf(cw_s[c * G + warp], cl_s[c * G + warp], l);
+    l = warp_sum(l);
+    if (lane == 0) gl_s[warp] = l;
+  }
+  __syncthreads();
+  constexpr int kQuads = D / 4;
+  for (int i = tid; i < G * kQuads; i += Tr::kThreads) {
+    const int g = i / kQuads, k4 = i - g * kQuads;
+    const float4* src =
+        reinterpret_cast<const float4*>(p.part_acc + (part_base * G + g) * D) + k4;
+    const int stride = G * kQuads;                                  // one split, in float4
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int c = 0; c < active; ++c) {
-      const float mc = __ldcg(&p.part_ml[((part_base + c) * G + g) * 2]);
-      const float f = mc == kNegInf ? 0.f : exp2f(mc - mx);
-      a = fmaf(f, __ldcg(&p.part_acc[((part_base + c) * G + g) * D + k]), a);
-      l = fmaf(f, __ldcg(&p.part_ml[((part_base + c) * G + g) * 2 + 1]), l);
+      const float w = cw_s[c * G + g];
+      const float4 v = __ldcg(src + static_cast<int64_t>(c) * stride);
+      a.x = fmaf(w, v.x, a.x);
+      a.y = fmaf(w, v.y, a.y);
+      a.z = fmaf(w, v.z, a.z);
+      a.w = fmaf(w, v.w, a.w);
     }
-    out_unit[i] = l > 0.f ? a / l : 0.f;
+    const float l = gl_s[g];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    reinterpret_cast<float4*>(out_unit + g * D)[k4] =
+        make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
   }
   if (tid == 0) p.counters[unit] = 0u;
+}
+
+template <bool BF16, int D, int G>
+std::atomic<unsigned long long>& attend_smem_flag() {
+  static std::atomic<unsigned long long> flag{0};
+  return flag;
+}
+
+// CTAs of this instantiation that fit on one SM (0 on error).
+template <bool BF16, int D, int G>
+int attend_resident_t() {
+  using Tr = AttendTraits<BF16, D, G>;
+  auto* kern = attend_kernel<BF16, D, G>;
+  if (ensure_dynamic_smem(kern, Tr::kSmem, attend_smem_flag<BF16, D, G>()) != cudaSuccess)
+    return 0;
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, Tr::kThreads, Tr::kSmem) !=
+      cudaSuccess)
+    return 0;
+  return blocks;
 }
 
 template <bool BF16, int D, int G>
@@ -412,8 +487,7 @@ cudaError_t launch_attend_t(const AttendParams& p, dim3 grid, bool programmatic,
                             cudaStream_t stream) {
   using Tr = AttendTraits<BF16, D, G>;
   auto* kern = attend_kernel<BF16, D, G>;
-  static std::atomic<unsigned long long> smem_set{0};
-  cudaError_t e = ensure_dynamic_smem(kern, Tr::kSmem, smem_set);
+  cudaError_t e = ensure_dynamic_smem(kern, Tr::kSmem, attend_smem_flag<BF16, D, G>());
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -441,6 +515,20 @@ cudaError_t launch_attend_g(const AttendParams& p, int group, dim3 grid, bool pr
     case 7: return launch_attend_t<BF16, D, 7>(p, grid, programmatic, stream);
     case 8: return launch_attend_t<BF16, D, 8>(p, grid, programmatic, stream);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool BF16, int D>
+int attend_resident_g(int group) {
+  switch (group) {
+    case 1: return attend_resident_t<BF16, D, 1>();
+    case 2: return attend_resident_t<BF16, D, 2>();
+    case 3: return attend_resident_t<BF16, D, 3>();
+    case 4: return attend_resident_t<BF16, D, 4>();
+    case 5: return attend_resident_t<BF16, D, 5>();
+    case 6: return attend_resident_t<BF16, D, 6>();
+    case 7: return attend_resident_t<BF16, D, 7>();
+    default: return attend_resident_t<BF16, D, 8>();
   }
 }
 

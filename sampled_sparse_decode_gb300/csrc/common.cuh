@@ -11,6 +11,8 @@ namespace santa {
 
 constexpr int kMaxGroup = 8;           // query heads per KV head supported by the kernels
 constexpr int kChunk = 64;             // tokens per staged K/V chunk
+constexpr int kMaxSplits = 256;        // split-K partials per unit (attention kernel)
+constexpr int kMaxChunksPerSplit = 256;  // 64-token chunks one attention CTA may own
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: no copy of ours takes that long
 
 __device__ __forceinline__ void set_status(int32_t* status, uint32_t bits) {

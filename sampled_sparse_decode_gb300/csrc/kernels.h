@@ -83,5 +83,8 @@ cudaError_t launch_attend_f32(const AttendParams& p, int head_dim, int group, di
                               bool programmatic, cudaStream_t stream);
 size_t attend_smem_bytes_bf16(int head_dim, int group);
 size_t attend_smem_bytes_f32(int head_dim, int group);
+int attend_resident_ctas(const AttendShape& s);
+int attend_resident_ctas_bf16(int head_dim, int group);
+int attend_resident_ctas_f32(int head_dim, int group);
 
 }  // namespace santa

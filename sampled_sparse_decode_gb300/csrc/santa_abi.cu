@@ -92,15 +92,37 @@ size_t ws_bytes_for(int64_t units, int G, int d, int splits) {
          static_cast<size_t>(units) * splits * G * d * sizeof(float);
 }
 
-// Default split: about four CTAs per SM over the whole job (two resident, two waves).
-int default_chunks_per_split(int64_t units, int64_t chunks_max, int sms) {
-  const int64_t target = std::max<int64_t>(1, static_cast<int64_t>(sms) * 4);
-  return static_cast<int>(std::max<int64_t>(1, ceil_div(units * chunks_max, target)));
-}
-
 int64_t chunks_max_of(int T, int max_teams, int M, bool dense) {
   const int64_t teams = dense ? max_teams : std::min(M, max_teams);
   return teams * (T / santa::kChunk);
+}
+
+// Splits needed so that no CTA owns more than kMaxChunksPerSplit chunks.
+int64_t min_splits_of(int64_t chunks_max) {
+  return ceil_div(chunks_max, santa::kMaxChunksPerSplit);
+}
+
+// Resident attention CTAs per SM for a shape (cached per device and shape).
+int resident_ctas(bool bf16, int d, int G) {
+  static std::mutex mu;
+  static int cache[64][2][2][santa::kMaxGroup + 1] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[dev][bf16 ? 1 : 0][d == 128 ? 1 : 0][G];
+  if (!c) c = std::max(1, santa::attend_resident_ctas(santa::AttendShape{bf16, d, G}));
+  return c;
+}
+
+// Default split: one wave of resident CTAs over the whole job, i.e. each unit gets
+// floor(SMs * resident / units) splits (at least one, at most kMaxSplits).
+void default_split(int64_t units, int64_t chunks_max, int sms, int resident, int64_t* cps,
+                   int64_t* splits) {
+  const int64_t slots = std::max<int64_t>(1, static_cast<int64_t>(sms) * resident);
+  const int64_t per_unit = std::min<int64_t>(santa::kMaxSplits, std::max<int64_t>(1, slots / units));
+  *cps = std::max<int64_t>(ceil_div(chunks_max, per_unit), 1);
+  *cps = std::min<int64_t>(*cps, santa::kMaxChunksPerSplit);
+  *splits = ceil_div(chunks_max, *cps);
 }
 
 struct Plan {
@@ -124,12 +146,12 @@ int make_plan(const santa_decode_args* a, bool dense, Plan* pl) {
   int64_t cap = static_cast<int64_t>((a->workspace_bytes - fixed - kAlign) /
                                      (static_cast<size_t>(units) * G * (d + 2) * sizeof(float)));
   const int64_t cmax = chunks_max_of(a->team_size, a->max_teams, a->num_draws, dense);
-  cap = std::min<int64_t>(cap, cmax);
-  if (cap < 1) return SANTA_ERR_INVALID_ARG;
+  cap = std::min<int64_t>({cap, cmax, static_cast<int64_t>(santa::kMaxSplits)});
+  if (cap < min_splits_of(cmax)) return SANTA_ERR_INVALID_ARG;
   const int sms = current_sms();
   if (sms <= 0) return SANTA_ERR_CUDA;
-  int64_t cps = default_chunks_per_split(units, cmax, sms);
-  int64_t splits = ceil_div(cmax, cps);
+  int64_t cps, splits;
+  default_split(units, cmax, sms, resident_ctas(a->dtype == SANTA_BF16, d, G), &cps, &splits);
   if (splits > cap) {
     cps = ceil_div(cmax, cap);
     splits = ceil_div(cmax, cps);
@@ -146,16 +168,17 @@ int make_plan(const santa_decode_args* a, bool dense, Plan* pl) {
   return SANTA_OK;
 }
 
-size_t default_ws_bytes(int batch, int hq, int hkv, int d, int T, int max_teams, int M,
-                        bool dense) {
-  if (check_shape(SANTA_F32, batch, hq, hkv, d, T, max_teams)) return 0;
+size_t default_ws_bytes(int dtype, int batch, int hq, int hkv, int d, int T, int max_teams,
+                        int M, bool dense) {
+  if (check_shape(dtype, batch, hq, hkv, d, T, max_teams)) return 0;
   if (!dense && (M < 1 || M > kMaxDraws)) return 0;
   const int64_t units = static_cast<int64_t>(batch) * hkv;
   const int G = hq / hkv;
   const int sms = current_sms();
   if (sms <= 0) return 0;
   const int64_t cmax = chunks_max_of(T, max_teams, M, dense);
-  const int64_t splits = ceil_div(cmax, default_chunks_per_split(units, cmax, sms));
+  int64_t cps, splits;
+  default_split(units, cmax, sms, resident_ctas(dtype == SANTA_BF16, d, G), &cps, &splits);
   return ws_bytes_for(units, G, d, static_cast<int>(splits));
 }
 
@@ -280,6 +303,11 @@ cudaError_t launch_attend(const AttendParams& p, const AttendShape& s, dim3 grid
                    : launch_attend_f32(p, s.head_dim, s.group, grid, programmatic, stream);
 }
 
+int attend_resident_ctas(const AttendShape& s) {
+  return s.is_bf16 ? attend_resident_ctas_bf16(s.head_dim, s.group)
+                   : attend_resident_ctas_f32(s.head_dim, s.group);
+}
+
 size_t attend_smem_bytes(const AttendShape& s) {
   return s.is_bf16 ? attend_smem_bytes_bf16(s.head_dim, s.group)
                    : attend_smem_bytes_f32(s.head_dim, s.group);
@@ -318,23 +346,29 @@ int santa_update_reps(const void* k_pool, int dtype, int64_t num_pages, int num_
                  page_fill, reps, device_status, static_cast<cudaStream_t>(stream));
 }
 
-size_t santa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
-                                    int team_size, int max_teams, int num_draws) {
-  return default_ws_bytes(batch, num_q_heads, num_kv_heads, head_dim, team_size, max_teams,
-                          num_draws, false);
+size_t santa_decode_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int team_size, int max_teams, int num_draws) {
+  return default_ws_bytes(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size,
+                          max_teams, num_draws, false);
 }
 
 size_t santa_decode_workspace_min_bytes(int batch, int num_q_heads, int num_kv_heads,
-                                        int head_dim) {
-  if (batch < 1 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads) return 0;
+                                        int head_dim, int team_size, int max_teams,
+                                        int num_draws) {
+  if (check_shape(SANTA_F32, batch, num_q_heads, num_kv_heads, head_dim, team_size, max_teams))
+    return 0;
+  if (num_draws < 1 || num_draws > kMaxDraws) return 0;
   const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
-  return kAlign + counters_bytes(units) + split_bytes(units, num_q_heads / num_kv_heads, head_dim);
+  const int64_t splits = min_splits_of(chunks_max_of(team_size, max_teams, num_draws, false));
+  return kAlign + counters_bytes(units) +
+         static_cast<size_t>(splits) * (split_bytes(units, num_q_heads / num_kv_heads, head_dim) -
+                                        kAlign) + kAlign;
 }
 
-size_t santa_dense_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
-                                   int team_size, int max_teams) {
-  return default_ws_bytes(batch, num_q_heads, num_kv_heads, head_dim, team_size, max_teams, 1,
-                          true);
+size_t santa_dense_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int team_size, int max_teams) {
+  return default_ws_bytes(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size,
+                          max_teams, 1, true);
 }
 
 int santa_sample(const santa_decode_args* a, void* stream) {

@@ -93,7 +93,10 @@ def test_reps_reject_bad_arguments_on_host(lib):
 def test_minimum_workspace_size(lib):
     f = lib.santa_decode_workspace_min_bytes
     f.restype = ctypes.c_size_t
-    f.argtypes = [ctypes.c_int] * 4
-    # 256 alignment slack + counters (rounded to 256) + one split: units*G*(d+2)*4 + 256
-    assert f(1, 28, 4, 128) == 256 + 256 + 4 * 7 * 130 * 4 + 256
-    assert f(1, 30, 4, 128) == 0
+    f.argtypes = [ctypes.c_int] * 7
+    # 256 alignment slack + counters (rounded to 256) + one split (<= 256 chunks of 64
+    # tokens each): units*G*(d+2)*4 + 256
+    assert f(1, 28, 4, 128, 128, 256, 31) == 256 + 256 + 4 * 7 * 130 * 4 + 256
+    # 4096 draws over 16384 teams of 128 tokens: 8192 chunks -> 32 splits
+    assert f(1, 28, 4, 128, 128, 16384, 4096) == 256 + 256 + 32 * 4 * 7 * 130 * 4 + 256
+    assert f(1, 30, 4, 128, 128, 256, 31) == 0

@@ -94,10 +94,12 @@ def test_workspace_of_minimum_size():
     cfg = wl.cfg
     full = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
                               cfg.draws, 3)
-    small = DecodeBuffers.allocate(cfg.batch, cfg.q_heads, cfg.kv_heads, cfg.head_dim,
-                                   cfg.team_size, dw.page_table.shape[1], cfg.draws)
+    mt = dw.page_table.shape[1]
+    small = DecodeBuffers.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads,
+                                   cfg.head_dim, cfg.team_size, mt, cfg.draws)
     small.workspace = torch.zeros(santa.santa_decode_workspace_min_bytes(
-        cfg.batch, cfg.q_heads, cfg.kv_heads, cfg.head_dim), dtype=torch.uint8, device="cuda")
+        cfg.batch, cfg.q_heads, cfg.kv_heads, cfg.head_dim, cfg.team_size, mt, cfg.draws),
+        dtype=torch.uint8, device="cuda")
     santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
                        cfg.draws, 3, bufs=small)
     torch.cuda.synchronize()
