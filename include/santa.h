@@ -69,7 +69,9 @@ typedef enum santa_status {
   SANTA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, short workspace */
   SANTA_ERR_UNSUPPORTED = 2,   /* a shape outside the supported set above */
   SANTA_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
-  SANTA_ERR_DEVICE_STATUS = 4  /* reserved for callers: *device_status was non-zero */
+  SANTA_ERR_DEVICE_STATUS = 4, /* reserved for callers: *device_status was non-zero */
+  SANTA_ERR_SCRATCH_LIMIT = 5  /* santa_decode_noalloc: the problem needs more scratch than
+                                  santa_noalloc_scratch_bytes() */
 } santa_status;
 
 typedef enum santa_dtype { SANTA_F32 = 0, SANTA_BF16 = 1 } santa_dtype;
@@ -194,6 +196,34 @@ int santa_decode(const santa_decode_args* a, void* stream);
 size_t santa_dense_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
                                    int head_dim, int team_size, int max_teams);
 int santa_dense_decode(const santa_decode_args* a, void* stream);
+
+/*
+ * santa_decode_noalloc — santa_decode for callers that cannot allocate device memory (no
+ * counterpart in the paper; it is a property of this library, not of the method).
+ *
+ * Who needs it: code that runs where cudaMalloc is not available or not allowed, such as
+ * a plug-in inside an inference engine that owns all device memory and lends none after
+ * start-up, or a loop that must not allocate once it is running.  Such a caller cannot
+ * provide santa_decode's workspace.  This entry point ignores a->workspace and
+ * a->workspace_bytes and uses instead a scratch array compiled into the library (a
+ * file-scope __device__ array of santa_noalloc_scratch_bytes() = 4 MiB, present on every
+ * device that loads the library until the process exits).  It calls no allocator.
+ *
+ *   - Same inputs, outputs and results as santa_decode (the split plan is the default one
+ *     cut down to fit the scratch, so the output may differ from santa_decode's in the
+ *     last bits only).
+ *   - Returns SANTA_ERR_SCRATCH_LIMIT, launching nothing, when the shape needs more than
+ *     the scratch holds (santa_decode_workspace_min_bytes > santa_noalloc_scratch_bytes).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array; the arrival counters in it are reset by
+ *     the sampling kernel of each call.  Calls whose kernels overlap on the GPU (different
+ *     streams, or other threads) race on it: serialise them.
+ */
+int santa_decode_noalloc(const santa_decode_args* a, void* stream);
+
+/* Size in bytes of the scratch array santa_decode_noalloc uses. */
+size_t santa_noalloc_scratch_bytes(void);
 
 #ifdef __cplusplus
 }

@@ -66,6 +66,8 @@ def lib():
             "santa_attend": (i32, [A, vp]),
             "santa_decode": (i32, [A, vp]),
             "santa_dense_decode": (i32, [A, vp]),
+            "santa_decode_noalloc": (i32, [A, vp]),
+            "santa_noalloc_scratch_bytes": (sz, []),
         }
         for name, (res, args) in sigs.items():
             f = getattr(L, name)
@@ -282,6 +284,21 @@ def santa_decode(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, 
     a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs)
     _check(lib().santa_decode(ctypes.byref(a), _stream(stream)), "santa_decode")
     return bufs
+
+
+def santa_decode_noalloc(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int,
+                         seed: int, bufs: DecodeBuffers, team_probs: bool = False,
+                         stream=None) -> DecodeBuffers:
+    """santa_decode with the library's built-in scratch instead of bufs.workspace, for
+    callers that cannot allocate device memory at call time (the caller still provides the
+    outputs in bufs; bufs.workspace is not used)."""
+    a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs)
+    _check(lib().santa_decode_noalloc(ctypes.byref(a), _stream(stream)), "santa_decode_noalloc")
+    return bufs
+
+
+def santa_noalloc_scratch_bytes() -> int:
+    return lib().santa_noalloc_scratch_bytes()
 
 
 def santa_dense_decode(q, k_pool, v_pool, page_table, seq_lens,

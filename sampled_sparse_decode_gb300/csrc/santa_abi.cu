@@ -326,6 +326,7 @@ const char* santa_status_string(int status) {
     case SANTA_ERR_UNSUPPORTED: return "unsupported shape (dtype, head_dim, team_size, group, draws or teams)";
     case SANTA_ERR_CUDA: return "CUDA runtime or launch error";
     case SANTA_ERR_DEVICE_STATUS: return "device status word reported an error";
+    case SANTA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than santa_decode_noalloc's static buffer holds";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,58 @@
+// santa_noalloc.cu — santa_decode for callers that cannot allocate device memory.
+//
+// santa_decode needs a caller-provided workspace for its split-K partials and arrival
+// counters.  Some callers cannot obtain one: code that runs where cudaMalloc is forbidden
+// or unavailable (a plug-in inside an inference engine that owns all device memory and
+// hands out none after start-up, a real-time loop that must not allocate once running,
+// or a runtime whose allocator is not reachable from C).  santa_decode_noalloc serves them
+// with a scratch buffer that lives in this library's own device image: a file-scope
+// __device__ array, created when the library's module is loaded on a device and held until
+// the process exits.  The call itself allocates nothing.
+#include <mutex>
+
+#include "kernels.h"
+
+namespace {
+
+// Upper bound of the scratch this entry point can use.  4 MiB holds the default split plan
+// of every workload in this repository (about 1 MiB each); larger problems run with fewer,
+// longer splits, and problems whose minimum need exceeds it are rejected.
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on each device, looked up once per device (the host
+// symbol itself is only a stand-in and must never be handed to a kernel).
+void* scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int santa_decode_noalloc(const santa_decode_args* a, void* stream) {
+  if (!a) return SANTA_ERR_INVALID_ARG;
+  const size_t need = santa_decode_workspace_min_bytes(a->batch, a->num_q_heads,
+                                                       a->num_kv_heads, a->head_dim,
+                                                       a->team_size, a->max_teams,
+                                                       a->num_draws);
+  if (need == 0) return SANTA_ERR_UNSUPPORTED;
+  if (need > kStaticScratchBytes) return SANTA_ERR_SCRATCH_LIMIT;
+  void* scratch = scratch_address();
+  if (!scratch) return SANTA_ERR_CUDA;
+  santa_decode_args b = *a;
+  b.workspace = scratch;
+  b.workspace_bytes = kStaticScratchBytes;
+  return santa_decode(&b, stream);
+}
+
+extern "C" size_t santa_noalloc_scratch_bytes(void) { return kStaticScratchBytes; }
