@@ -63,7 +63,9 @@ def lib():
             "oracle_elem": (dbl, [vp, i32, i64]),
             "oracle_build_reps": (i32, [P, vp, vp]),
             "oracle_team_probs": (i32, [P, vp, i32, i32, vp, vp]),
-            "oracle_cdf_search": (i32, [vp, i32, dbl]),
+            "oracle_cdf_search": (i32, [vp, i32, u64]),
+            "oracle_fixed_prob": (u64, [dbl]),
+            "oracle_draw_point": (u64, [u64, i32, i32, i32, u64]),
             "oracle_draw": (None, [vp, i32, i32, u64, i32, i32, vp, vp, vp]),
             "oracle_select": (i32, [vp, i32, vp, i32, vp, vp]),
             "oracle_num_den": (i32, [P, i32, i32, vp, vp, i32, vp, vp, vp]),
@@ -158,18 +160,27 @@ def team_probs(pr: Problem, reps: np.ndarray, b: int, h: int, with_scores: bool 
     return (p[:n], s[:, :n]) if with_scores else p[:n]
 
 
-def cdf_search(C: np.ndarray, t: float) -> int:
-    C = np.ascontiguousarray(C, dtype=np.float64)
-    return lib().oracle_cdf_search(_ptr(C), C.size, t)
+def cdf_search(C: np.ndarray, t: int) -> int:
+    C = np.ascontiguousarray(C, dtype=np.uint64)
+    return lib().oracle_cdf_search(_ptr(C), C.size, int(t))
+
+
+def fixed_prob(p: float) -> int:
+    return int(lib().oracle_fixed_prob(float(p)))
+
+
+def draw_point(seed: int, b: int, h: int, r: int, Z: int) -> int:
+    return int(lib().oracle_draw_point(seed, b, h, r, int(Z)))
 
 
 def draw(p: np.ndarray, M: int, seed: int, b: int, h: int):
-    """Returns (draws [M] int32, t = u*Z [M], C [n])."""
+    """Returns (draws [M] int32, t = floor(u*Z) [M] uint64, C [n] uint64), with C the
+    fixed-point (2^62) integer CDF."""
     p = np.ascontiguousarray(p, dtype=np.float64)
     n = p.size
     draws = np.zeros(M, dtype=np.int32)
-    t = np.zeros(M, dtype=np.float64)
-    C = np.zeros(n, dtype=np.float64)
+    t = np.zeros(M, dtype=np.uint64)
+    C = np.zeros(n, dtype=np.uint64)
     lib().oracle_draw(_ptr(p), n, M, seed, b, h, _ptr(draws), _ptr(t), _ptr(C))
     return draws, t, C
 

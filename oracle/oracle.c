@@ -21,14 +21,17 @@
  *   - the M draws are i.i.d. with replacement; draw r of unit (b, h) takes word 0 of
  *     Philox4x32-10 with key (lo32(seed), hi32(seed)) and counter (r, h, b, 0), maps it to
  *     u = (x + 0.5) / 2^32 and picks the smallest i with u*Z < C_i (strict), C the running
- *     sum of p in team order and Z = C_{n-1};
+ *     sum of p in team order and Z = C_{n-1}; the pages fix no arithmetic for this
+ *     decision, and it is taken exactly on 62-bit fixed-point probabilities (integer CDF,
+ *     floor(u Z) by a 128-bit product), the same way the GPU kernel takes it;
  *   - S is the set of distinct drawn teams and the weight of team i is 1/pi_i with
  *     pi_i = 1 - (1 - p_i)^M, the probability that i is drawn at least once (Horvitz-
  *     Thompson), applied to numerator and denominator alike; the output is their ratio.
  *
  * Data: q [B][Hq][d], k_pool / v_pool [P][Hkv][T][d] in fp32 or bf16 (read exactly into
  * double), page_table [B][max_teams], seq_lens [B].  Every floating-point step is fp64.
- * Build: gcc -O2 -ffp-contract=off (no contraction, so results do not depend on the host).
+ * Build: gcc -O2 -ffp-contract=off (no contraction, so results do not depend on the host);
+ * the sampling decision uses unsigned __int128 (gcc, x86-64 and aarch64).
  */
 #include <math.h>
 #include <stdint.h>
@@ -120,7 +123,8 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t
 }
 
 /* The uniform of draw r of unit (b, h): word 0 of Philox4x32-10 at counter (r, h, b, 0)
- * under key (lo32(seed), hi32(seed)), as (x + 1/2) / 2^32, which is exact in fp64. */
+ * under key (lo32(seed), hi32(seed)), as (x + 1/2) / 2^32, which is exact in fp64.  (The
+ * draws use it exactly, through oracle_draw_point.) */
 double oracle_uniform(uint64_t seed, int b, int h, int r) {
   uint32_t ctr[4] = {(uint32_t)r, (uint32_t)h, (uint32_t)b, 0u};
   uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
@@ -195,9 +199,16 @@ int oracle_team_probs(const oracle_problem* pr, const double* reps, int b, int h
 
 /* ---------------------------------------------------------------- step 3: sampling */
 
+/* Team probability as a 62-bit fixed-point integer: round(p * 2^62), ties away from zero.
+ * The CDF is the exact integer running sum of these, so its value does not depend on the
+ * order of the additions. */
+uint64_t oracle_fixed_prob(double p) {
+  return (uint64_t)llround(ldexp(p, 62));
+}
+
 /* Inverse-CDF search: the smallest i with t < C[i]; if there is none (t >= C[n-1]), the
  * smallest i with C[i] == C[n-1], i.e. the team that completes the distribution. */
-int oracle_cdf_search(const double* C, int n, double t) {
+int oracle_cdf_search(const uint64_t* C, int n, uint64_t t) {
   for (int i = 0; i < n; ++i)
     if (t < C[i]) return i;
   for (int i = 0; i < n; ++i)
@@ -205,23 +216,36 @@ int oracle_cdf_search(const double* C, int n, double t) {
   return n - 1;
 }
 
+/* Position of draw r on the integer CDF: t = floor(u * Z) with u = (2x + 1) / 2^33, x the
+ * draw's Philox word, computed exactly with a 128-bit product.  t < Z always. */
+uint64_t oracle_draw_point(uint64_t seed, int b, int h, int r, uint64_t Z) {
+  uint32_t ctr[4] = {(uint32_t)r, (uint32_t)h, (uint32_t)b, 0u};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t w[4];
+  oracle_philox4x32_10(ctr, key, w);
+  unsigned __int128 prod = (unsigned __int128)(2ull * w[0] + 1ull) * Z;
+  return (uint64_t)(prod >> 33);
+}
+
 /* M i.i.d. draws from p[0..n) for unit (b, h), 1 <= n <= ORACLE_MAX_TEAMS.
- * [ABS; EXP 三 step 3]
- * draws [M] receive team indices; t_out [M] (may be NULL) receives u*Z; cdf [n] (may be
- * NULL) receives C. */
+ * [ABS; EXP 三 step 3]  The draw takes u = (x + 1/2) / 2^32 and picks the smallest i with
+ * u * Z < C_i, evaluated exactly on the fixed-point CDF (C_i = sum_{k<=i} round(p_k 2^62),
+ * Z = C_{n-1}).
+ * draws [M] receive team indices; t_out [M] (may be NULL) receives floor(u * Z); cdf [n]
+ * (may be NULL) receives C. */
 void oracle_draw(const double* p, int n, int M, uint64_t seed, int b, int h, int32_t* draws,
-                 double* t_out, double* cdf) {
+                 uint64_t* t_out, uint64_t* cdf) {
   if (n < 1 || n > ORACLE_MAX_TEAMS) return;
-  double* C = (double*)malloc(sizeof(double) * (size_t)n);
+  uint64_t* C = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)n);
   if (!C) return;
-  double run = 0.0;
+  uint64_t run = 0;
   for (int i = 0; i < n; ++i) {
-    run += p[i];
+    run += oracle_fixed_prob(p[i]);
     C[i] = run;
   }
-  const double Z = C[n - 1];
+  const uint64_t Z = C[n - 1];
   for (int r = 0; r < M; ++r) {
-    double t = oracle_uniform(seed, b, h, r) * Z;
+    const uint64_t t = oracle_draw_point(seed, b, h, r, Z);
     draws[r] = oracle_cdf_search(C, n, t);
     if (t_out) t_out[r] = t;
   }

@@ -13,8 +13,9 @@ from sampled_sparse_decode_gb300 import workloads as W
 # Output tolerances (max-abs), for outputs computed on identical sampled sets: fp32 inputs
 # with fp32 arithmetic, and bf16 inputs with fp32 accumulation.
 TOL_OUT = {"f32": 1e-5, "bf16": 2e-3}
-# A draw may differ from the oracle's only if the oracle's u*Z lies this close to one of the
-# oracle's CDF values (fp32 team probabilities on the GPU, fp64 in the oracle) ...
+# A draw may differ from the oracle's only if the oracle's u*Z lies this close (relative to
+# Z) to one of the oracle's CDF values (the team probabilities come from fp32 scores on the
+# GPU and fp64 ones in the oracle; the decision itself is exact integer arithmetic on both) ...
 BOUNDARY_WINDOW = 1e-6
 # ... and such draws must stay below this share of all draws.
 BOUNDARY_SHARE = 1e-4
@@ -56,16 +57,20 @@ def full_oracle_reps(name: str) -> np.ndarray:
     return oracle.build_reps(problem(wl), wl.page_fill)
 
 
-def boundary_distance(t: float, C: np.ndarray) -> float:
-    """Distance from t to the nearest CDF value (the interval boundaries)."""
-    return float(np.min(np.abs(C - t))) if C.size else float("inf")
+def boundary_distance(t: int, C: np.ndarray) -> float:
+    """Distance from the draw point t to the nearest CDF value (an interval boundary), in
+    units of the CDF total Z (t and C are the oracle's fixed-point integers)."""
+    if not C.size:
+        return float("inf")
+    Cf = C.astype(np.float64)
+    return float(np.min(np.abs(Cf - float(t)))) / float(Cf[-1])
 
 
 def compare_draws(gpu_draws: np.ndarray, ora_draws: np.ndarray, t: np.ndarray, C: np.ndarray):
     """Returns (mismatches inside the boundary window, mismatches outside it)."""
     inside = outside = 0
     for r in np.nonzero(gpu_draws != ora_draws)[0]:
-        if boundary_distance(t[r], C) <= BOUNDARY_WINDOW:
+        if boundary_distance(int(t[r]), C) <= BOUNDARY_WINDOW:
             inside += 1
         else:
             outside += 1

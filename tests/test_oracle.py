@@ -201,13 +201,45 @@ def test_team_probs_follow_the_page_table():
 # ------------------------------------------------------------------ sampling
 
 def test_cdf_search_is_strict_and_skips_empty_teams():
-    C = np.array([0.25, 0.25, 0.5, 1.0])              # team 1 has probability 0
-    assert oracle.cdf_search(C, 0.0) == 0
-    assert oracle.cdf_search(C, 0.2499999) == 0
-    assert oracle.cdf_search(C, 0.25) == 2             # boundary belongs to the next team
-    assert oracle.cdf_search(C, 0.75) == 3
-    assert oracle.cdf_search(C, 1.0) == 3              # t >= Z: the completing team
-    assert oracle.cdf_search(np.array([0.5, 1.0, 1.0]), 1.0) == 1
+    C = np.array([25, 25, 50, 100], dtype=np.uint64)   # team 1 has probability 0
+    assert oracle.cdf_search(C, 0) == 0
+    assert oracle.cdf_search(C, 24) == 0
+    assert oracle.cdf_search(C, 25) == 2               # boundary belongs to the next team
+    assert oracle.cdf_search(C, 75) == 3
+    assert oracle.cdf_search(C, 100) == 3              # t >= Z: the completing team
+    assert oracle.cdf_search(np.array([50, 100, 100], dtype=np.uint64), 100) == 1
+
+
+def test_fixed_point_probabilities_round_half_away():
+    assert oracle.fixed_prob(1.0) == 2**62
+    assert oracle.fixed_prob(0.5) == 2**61
+    assert oracle.fixed_prob(0.0) == 0
+    assert oracle.fixed_prob(2.0**-63) == 1             # 0.5 rounds away from zero
+    assert oracle.fixed_prob(2.0**-64) == 0             # 0.25 rounds to 0
+    assert oracle.fixed_prob(3 * 2.0**-63) == 2         # 1.5 rounds to 2
+
+
+def test_draws_are_exact_on_the_integer_cdf():
+    """The draws equal an independent exact evaluation: Python integers for the fixed-point
+    CDF and for floor(u Z) with u = (2x + 1) / 2^33, and bisect for the smallest team with
+    t < C_i; the Philox words come from the pinned generator."""
+    import bisect
+    from fractions import Fraction
+    rng = np.random.default_rng(3)
+    for n, seed, b, h in [(7, 5, 0, 0), (64, 2**40 + 3, 3, 2), (300, 11, 1, 5)]:
+        p = rng.dirichlet(np.full(n, 0.3))
+        p[rng.integers(0, n)] = 0.0
+        P = [int(Fraction(float(x)) * 2**62 + Fraction(1, 2)) for x in p]
+        C = list(__import__("itertools").accumulate(P))
+        Z = C[-1]
+        M = 500
+        draws, t, Co = oracle.draw(p, M, seed, b, h)
+        assert [int(c) for c in Co] == C
+        for r in range(M):
+            x = int(oracle.philox4x32_10([r, h, b, 0], [seed & 0xFFFFFFFF, seed >> 32])[0])
+            tr = ((2 * x + 1) * Z) >> 33
+            assert int(t[r]) == tr
+            assert draws[r] == bisect.bisect_right(C, tr)
 
 
 def test_draw_frequencies_follow_p():
@@ -220,7 +252,7 @@ def test_draw_frequencies_follow_p():
     assert counts[2] == 0
     nz = p > 0
     assert stats.chisquare(counts[nz], p[nz] * draws.size).pvalue > 1e-4
-    np.testing.assert_allclose(C, np.cumsum(p), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(C.astype(np.float64) / 2.0**62, np.cumsum(p), rtol=0, atol=1e-15)
 
 
 def test_inclusion_probability_golden():
