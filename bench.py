@@ -6,15 +6,15 @@
 
 Workload: the Qwen2.5-7B-shaped decode attention layer at 32K context (1 sequence, 28 query
 / 4 KV heads, d = 128, T = 128, M = 31 draws, bf16 K/V, mixture keys), seeded synthetic
-data.  A step is one SANTA++ decode step: team scoring + sampling (santa_sample's kernel)
-and the split-K Horvitz-Thompson attention (santa_attend's kernel), through santa_decode.
+data.  A step is one SANTA++ decode step through santa_decode: one launch of the fused kernel
+(team scoring and sampling, then split-K Horvitz-Thompson attention over the sampled teams).
 
 value      steps/s of whole decode steps with inputs resident in HBM, K steps replayed from
            CUDA graphs; the K/V/representative buffers rotate over R copies so that the
            bytes touched between two uses of a copy exceed 6x the L2 size.
-roofline   the attention kernel (the dominant one): algorithmic bytes per launch (K and V of
-           the sampled teams, q, out) / its mean duration (CUDA events, graph-replayed
-           launches), against the measured HBM copy bandwidth.
+roofline   the fused decode kernel (one launch per step): algorithmic bytes per launch (the
+           team representatives, K and V of the sampled teams, q, out) / its mean duration
+           (CUDA events over graph-replayed launches), against the measured HBM copy bandwidth.
 e2e        the same steps through the Python API with pinned host buffers: per step the
            query, page table and lengths go host->device and out, draw/sampled ids, pi and
            |S| come back device->host, then the stream is synchronised.
@@ -41,8 +41,8 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn steps/s and achieved HBM GB/s at 32K ctx, M=31/64 teams, 1 GB300"
 DEFAULT_WORKLOAD = "qwen7b_32k_b1_m31"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_traffic.json")
-ATTEND_SOURCES = ["sampled_sparse_decode_gb300/csrc/attend_kernel.cuh",
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+KERNEL_SOURCES = ["sampled_sparse_decode_gb300/csrc/decode_kernel.cuh",
                   "sampled_sparse_decode_gb300/csrc/common.cuh"]
 
 
@@ -81,21 +81,21 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def attend_source_sha():
+def kernel_source_sha():
     h = hashlib.sha256()
-    for rel in ATTEND_SOURCES:
+    for rel in KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload):
-    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on
-    the current kernel source and this workload (else None)."""
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current kernel source and this workload (else None)."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
-        if rec.get("kernel_source_sha") == attend_source_sha() and rec.get("workload") == workload:
+        if rec.get("kernel_source_sha") == kernel_source_sha() and rec.get("workload") == workload:
             return float(rec["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -356,18 +356,12 @@ def run_ours(args):
     mean_sel = sel_total / (R * units)
     assert int(bufs.device_status.item()) == 0
 
-    # ---- the attention kernel alone (sampled sets of the last seed)
-    sec_a, n_a, _ = timed(rounds(lib.santa_attend, args_r), K, W_)
-    att_s = sec_a / n_a
-    with torch.cuda.stream(stream):
-        call(lib.santa_sample, args_r[R - 1])
-        stream.synchronize()
-    sel_last = int(bufs.sel_count.sum().item())
-    # attention-kernel algorithmic bytes: K and V of the sampled teams (valid tokens), q, out
-    att_bytes = sel_last * T * 2 * d * esize + cfg.batch * cfg.q_heads * d * (esize + 4)
-    # the sampling kernel alone (for the launch breakdown)
+    # ---- the two halves alone, for the breakdown: sampling only, attention only (on the
+    # sampled sets of the last seed)
     sec_s, n_s, _ = timed(rounds(lib.santa_sample, args_r), K, W_)
     smp_s = sec_s / n_s
+    sec_a, n_a, _ = timed(rounds(lib.santa_attend, args_r), K, W_)
+    att_s = sec_a / n_a
 
     # ---- dense split-K reference on the same buffers
     sec_d, n_d, _ = timed(rounds(lib.santa_dense_decode, dargs_r), max(R, K // 4), W_)
@@ -375,12 +369,13 @@ def run_ours(args):
     clocks.stop()
     clk = clocks.summary(c0, c1)
 
-    # ---- bytes per step (realised |S|): reps of every team, K/V of the sampled teams, q, out
+    # ---- algorithmic bytes per step (realised |S|): the representatives of every team, K
+    # and V of the sampled teams, q and out.  One launch of the fused kernel per step.
     step_bytes = (units * n_teams * d * 4 + mean_sel * units * T * 2 * d * esize +
                   cfg.batch * cfg.q_heads * d * (esize + 4))
     dense_kv = units * cfg.seq_len * 2 * d * esize
     peak, peak_kind = measured_peak()
-    achieved = att_bytes / att_s / 1e9
+    achieved = step_bytes / step_s / 1e9
 
     # ---- end to end through the Python API, host buffers
     e2e = None
@@ -456,16 +451,17 @@ def run_ours(args):
         "dense": {"steps_per_s": 1.0 / dense_s, "latency_us": dense_s * 1e6,
                   "hbm_gbs": dense_kv / dense_s / 1e9},
         "speedup_vs_dense": dense_s / step_s,
-        "kernels_us": {"score_sample": smp_s * 1e6, "attend": att_s * 1e6,
-                       "dense_attend": dense_s * 1e6},
+        "kernels_us": {"decode": step_s * 1e6, "sample_only": smp_s * 1e6,
+                       "attend_only": att_s * 1e6, "dense": dense_s * 1e6},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "attend_kernel (split-K Horvitz-Thompson attention)",
-                     "bytes_per_launch": att_bytes,
+                     "kernel": "decode_kernel (fused sampling + split-K HT attention), "
+                               "one launch per step",
+                     "bytes_per_launch": step_bytes,
                      "traffic": recorded_traffic(cfg.name)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * steps_done,
+        "gpu_launches": steps_done,
         "clocks": clk,
     }
     print(json.dumps(line))

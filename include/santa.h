@@ -142,19 +142,23 @@ typedef struct santa_decode_args {
   int32_t* sel_count;
   float* pi;
   float* team_probs;           /* optional, may be NULL */
-  /* scratch: caller-owned device memory, contents need not be initialised */
+  /* scratch: caller-owned device memory (see "Workspace" below), zeroed before first use */
   void* workspace;
   size_t workspace_bytes;
   int32_t* device_status;      /* one int32 the kernels OR SANTA_DEV_* bits into */
 } santa_decode_args;
 
 /*
- * Workspace for santa_attend / santa_decode: split-K partials (m, l, acc[d]) per query head
- * and one arrival counter per unit.  santa_decode_workspace_bytes returns the size of the
- * library's default split plan on the current device (one wave of resident attention CTAs;
- * 0 for an unsupported shape); any size down to santa_decode_workspace_min_bytes also works,
- * with fewer, longer splits.  The workspace of santa_dense_decode is sized the same way by
- * santa_dense_workspace_bytes.  A workspace is used by one call at a time.
+ * Workspace.  A unit is served by one thread-block cluster (up to 16 CTAs sharing their
+ * partial results on chip) unless it has so much work that several clusters share it;
+ * only then do the clusters' partials and an arrival counter per unit go through the
+ * workspace.  santa_decode_workspace_bytes returns the size the library's default plan
+ * wants on the current device (0 for an unsupported shape); any size down to
+ * santa_decode_workspace_min_bytes also works, with fewer clusters per unit.  When the
+ * minimum is 256 bytes (every unit fits one cluster), the workspace may be NULL.  The
+ * counters must be zero before the first call (they are left at zero by every call).
+ * santa_dense_workspace_bytes sizes the workspace of santa_dense_decode the same way.  A
+ * workspace is used by one call at a time.
  */
 size_t santa_decode_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
                                     int head_dim, int team_size, int max_teams, int num_draws);
@@ -165,9 +169,9 @@ size_t santa_decode_workspace_min_bytes(int batch, int num_q_heads, int num_kv_h
 /*
  * santa_sample — score the representatives, form the GQA-mixed team distribution, draw M
  * teams, deduplicate and compute the inclusion probabilities.  Writes draw_ids, sel_ids,
- * sel_count, pi, team_probs (if not NULL) and resets the unit counters in the workspace.
+ * sel_count, pi and team_probs (if not NULL).
  * [ABS: "the query scores one representative from each team to decide which teams to
- * sample"; EXP section 三 steps 2-3.]
+ * sample"; EXP section 三 steps 2-3.]  Uses no workspace.
  */
 int santa_sample(const santa_decode_args* a, void* stream);
 
@@ -176,12 +180,20 @@ int santa_sample(const santa_decode_args* a, void* stream);
  * unit, each team weighted by 1/pi, combined as the Horvitz-Thompson ratio into out.
  * sel_ids / sel_count / pi may come from santa_sample or from the caller (distinct team
  * indices < n, any order, 0 < pi <= 1); entries out of range set SANTA_DEV_BAD_SEL and are
- * skipped.  The workspace counters must have been reset by santa_sample on the same
- * workspace, or the caller must zero the whole workspace first.
+ * skipped.
  * [ABS: "We compute exact attention scores within the sampled teams and reweight each
  * team's contribution by the inverse of its inclusion probability"; EXP steps 4-5.]
  */
 int santa_attend(const santa_decode_args* a, void* stream);
+
+/*
+ * santa_decode_plan — the launch the library would use for `a` (whose pointers need not be
+ * valid; only shapes and workspace_bytes are read): out[0] = CTAs per thread-block cluster
+ * (CL), out[1] = clusters per unit (NC; NC > 1 routes partials through the workspace),
+ * out[2] = teams one CTA scores, out[3] = clusters of CL CTAs the device can run at once.
+ * `which`: 0 santa_decode, 1 santa_sample, 2 santa_attend, 3 santa_dense_decode.
+ */
+int santa_decode_plan(const santa_decode_args* a, int which, int32_t* out);
 
 /* santa_decode — santa_sample followed by santa_attend on `stream`. [ABS] */
 int santa_decode(const santa_decode_args* a, void* stream);

@@ -67,6 +67,7 @@ def lib():
             "santa_decode": (i32, [A, vp]),
             "santa_dense_decode": (i32, [A, vp]),
             "santa_decode_noalloc": (i32, [A, vp]),
+            "santa_decode_plan": (i32, [A, i32, vp]),
             "santa_noalloc_scratch_bytes": (sz, []),
         }
         for name, (res, args) in sigs.items():
@@ -295,6 +296,33 @@ def santa_decode_noalloc(q, k_pool, v_pool, reps, page_table, seq_lens, num_draw
     a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs)
     _check(lib().santa_decode_noalloc(ctypes.byref(a), _stream(stream)), "santa_decode_noalloc")
     return bufs
+
+
+_PLAN_MODES = {"decode": 0, "sample": 1, "attend": 2, "dense": 3}
+
+
+def santa_decode_plan(q, k_pool, page_table, num_draws: int, which: str = "decode",
+                      workspace_bytes: int | None = None) -> dict:
+    """The launch shape the library picks: cluster size, clusters per unit, teams per CTA
+    and the device's co-resident cluster count for that size."""
+    B, Hq, d = q.shape
+    _, Hkv, T, _ = k_pool.shape
+    a = _DecodeArgs()
+    a.dtype, a.batch, a.num_q_heads, a.num_kv_heads = _DTYPES[q.dtype], B, Hq, Hkv
+    a.head_dim, a.team_size, a.max_teams, a.num_draws = d, T, page_table.shape[1], num_draws
+    a.num_pages = k_pool.shape[0]
+    if workspace_bytes is None:
+        workspace_bytes = (santa_dense_workspace_bytes(q.dtype, B, Hq, Hkv, d, T,
+                                                       page_table.shape[1])
+                           if which == "dense" else
+                           santa_decode_workspace_bytes(q.dtype, B, Hq, Hkv, d, T,
+                                                        page_table.shape[1], num_draws))
+    a.workspace = 256 if workspace_bytes else None        # only its size is read
+    a.workspace_bytes = workspace_bytes
+    out = (ctypes.c_int32 * 4)()
+    _check(lib().santa_decode_plan(ctypes.byref(a), _PLAN_MODES[which], out), "santa_decode_plan")
+    return {"cluster": out[0], "clusters_per_unit": out[1], "teams_per_cta": out[2],
+            "max_active_clusters": out[3]}
 
 
 def santa_noalloc_scratch_bytes() -> int:

@@ -11,8 +11,10 @@ namespace santa {
 
 constexpr int kMaxGroup = 8;           // query heads per KV head supported by the kernels
 constexpr int kChunk = 64;             // tokens per staged K/V chunk
-constexpr int kMaxSplits = 256;        // split-K partials per unit (attention kernel)
-constexpr int kMaxChunksPerSplit = 256;  // 64-token chunks one attention CTA may own
+constexpr int kMaxChunksPerSplit = 256;  // 64-token chunks one CTA may own
+constexpr int kMaxTeamsPerCta = 1024;    // teams one CTA scores and samples
+constexpr int kMaxCluster = 16;          // CTAs per cluster (non-portable above 8)
+constexpr int kMaxClustersPerUnit = 16;  // clusters serving one unit
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: no copy of ours takes that long
 
 __device__ __forceinline__ void set_status(int32_t* status, uint32_t bits) {
@@ -107,19 +109,6 @@ inline cudaError_t ensure_dynamic_smem(Kernel* kernel, size_t bytes,
                            static_cast<int>(bytes));
   if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
-}
-
-// ---------------------------------------------------------------- programmatic launch
-
-// Lets the next kernel on the stream (launched with programmatic stream serialization)
-// begin its prologue.
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-// Waits until the preceding kernel on the stream has completed and its writes are visible
-// (a no-op when this kernel was not launched as a programmatic dependent).
-__device__ __forceinline__ void pdl_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- warp reductions

@@ -23,68 +23,46 @@ struct RepsParams {
 };
 cudaError_t launch_reps(const RepsParams& p, int head_dim, cudaStream_t stream);
 
-// ---------------------------------------------------------------- score + sample
-struct SampleParams {
-  const void* q;
-  const float* reps;
-  const int32_t* page_table;
-  const int32_t* seq_lens;
-  bool is_bf16;
-  int batch, num_q_heads, num_kv_heads, group, team_size, max_teams, num_draws;
-  int64_t num_pages;
-  uint64_t seed;
-  float scale;              // 1/sqrt(d)
-  int teams_per_cta;        // shared-memory capacity: ceil(max_teams / cluster size)
-  int32_t* draw_ids;
-  int32_t* sel_ids;
-  int32_t* sel_count;
-  float* pi;
-  float* team_probs;        // may be nullptr
-  uint32_t* counters;       // [B*Hkv] split-arrival counters to reset (may be nullptr)
-  int32_t* status;
-};
-size_t sample_smem_bytes(int head_dim, int teams_per_cta);
-cudaError_t launch_sample(const SampleParams& p, int head_dim, int cluster, cudaStream_t stream);
+// ---------------------------------------------------------------- fused decode step
+constexpr int kModeDecode = 0;   // sample, then attend over the sampled teams
+constexpr int kModeSample = 1;   // sample only
+constexpr int kModeAttend = 2;   // attend over the caller's sel_ids / sel_count / pi
+constexpr int kModeDense = 3;    // attend over every team with weight 1
 
-// ---------------------------------------------------------------- split-K attention
-struct AttendParams {
+struct DecodeParams {
   const void* q;
   const void* k_pool;
   const void* v_pool;
+  const float* reps;
   const int32_t* page_table;
   const int32_t* seq_lens;
-  const int32_t* sel_ids;   // sampled mode: [B*Hkv][M]
-  const int32_t* sel_count; // sampled mode: [B*Hkv]
-  const float* pi;          // sampled mode: [B*Hkv][M]
   int batch, num_q_heads, num_kv_heads, team_size, max_teams, num_draws;
   int64_t num_pages;
-  float scale_log2;         // log2(e) / sqrt(d): scores live in the base-2 domain
-  int dense;                // 1: every token of every team, weight 1
-  int chunks_per_split;     // 64-token chunks handled by one CTA
-  int max_splits;           // splits held per unit by the workspace
-  float* part_ml;           // [B*Hkv][max_splits][G][2]  (running max, running sum)
-  float* part_acc;          // [B*Hkv][max_splits][G][d]
-  uint32_t* counters;       // [B*Hkv] arrival counters, zero between calls
+  uint64_t seed;
+  float scale;              // 1/sqrt(d): representative scores (natural base)
+  float scale_log2;         // log2(e)/sqrt(d): in-team scores (base 2)
+  int mode;                 // kMode*
+  int teams_per_cta;        // sampling: ceil(max_teams / cluster size) <= kMaxTeamsPerCta
+  int clusters_per_unit;    // NC
   float* out;               // [B][Hq][d]
+  int32_t* draw_ids;        // [B*Hkv][M]
+  int32_t* sel_ids;         // [B*Hkv][M]  (read in attend mode)
+  int32_t* sel_count;       // [B*Hkv]     (read in attend mode)
+  float* pi;                // [B*Hkv][M]  (read in attend mode)
+  float* team_probs;        // [B*Hkv][max_teams] or nullptr
+  float* part_ml;           // NC > 1: [B*Hkv][NC][G][2]
+  float* part_acc;          // NC > 1: [B*Hkv][NC][G][d]
+  uint32_t* counters;       // NC > 1: [B*Hkv], zero between calls
   int32_t* status;
 };
-struct AttendShape {
-  bool is_bf16;
-  int head_dim;
-  int group;
-};
-size_t attend_smem_bytes(const AttendShape& s);
-cudaError_t launch_attend(const AttendParams& p, const AttendShape& s, dim3 grid,
-                          bool programmatic, cudaStream_t stream);
-// per-dtype launchers (one translation unit each)
-cudaError_t launch_attend_bf16(const AttendParams& p, int head_dim, int group, dim3 grid,
-                               bool programmatic, cudaStream_t stream);
-cudaError_t launch_attend_f32(const AttendParams& p, int head_dim, int group, dim3 grid,
-                              bool programmatic, cudaStream_t stream);
-size_t attend_smem_bytes_bf16(int head_dim, int group);
-size_t attend_smem_bytes_f32(int head_dim, int group);
-int attend_resident_ctas(const AttendShape& s);
-int attend_resident_ctas_bf16(int head_dim, int group);
-int attend_resident_ctas_f32(int head_dim, int group);
+
+cudaError_t decode_launch_bf16(const DecodeParams& p, int head_dim, int group, dim3 grid,
+                               int cluster, cudaStream_t stream);
+cudaError_t decode_launch_f32(const DecodeParams& p, int head_dim, int group, dim3 grid,
+                              int cluster, cudaStream_t stream);
+int decode_resident_bf16(int head_dim, int group);
+int decode_resident_f32(int head_dim, int group);
+int decode_max_clusters_bf16(int head_dim, int group, int cluster);
+int decode_max_clusters_f32(int head_dim, int group, int cluster);
 
 }  // namespace santa

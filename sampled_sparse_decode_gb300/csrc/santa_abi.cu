@@ -11,10 +11,8 @@
 
 namespace {
 
-using santa::AttendParams;
-using santa::AttendShape;
+using santa::DecodeParams;
 using santa::RepsParams;
-using santa::SampleParams;
 
 constexpr int kMaxTeams = 16384;
 constexpr int kMaxDraws = 4096;
@@ -74,198 +72,221 @@ int check_draws(const santa_decode_args* a) {
   return SANTA_OK;
 }
 
-// ---------------------------------------------------------------- workspace and split plan
+// ---------------------------------------------------------------- launch plan
 //
-// Workspace layout (base rounded up to 256 bytes):
+// A unit (sequence, KV head) is served by NC clusters of CL CTAs.  CL is the largest power
+// of two <= 16 that keeps the whole job within one wave of resident CTAs (and that the
+// device can co-schedule); sampling needs CL >= max_teams / 1024.  NC > 1 only when one
+// cluster would give each CTA more than 8 chunks and the wave has room, or when a CTA would
+// own more than kMaxChunksPerSplit chunks.  Only NC > 1 uses the workspace:
 //   counters  [B*Hkv] uint32                      (rounded up to 256 bytes)
-//   part_ml   [B*Hkv][cap][G][2] fp32 (m, l)       (rounded up to 256 bytes)
-//   part_acc  [B*Hkv][cap][G][d] fp32
-// where cap, the splits a unit may use, is whatever the given size holds.
+//   part_ml   [B*Hkv][NC][G][2] fp32 (m, l)       (rounded up to 256 bytes)
+//   part_acc  [B*Hkv][NC][G][d] fp32
+// with the base rounded up to 256 bytes.
 
 size_t counters_bytes(int64_t units) { return round_up(static_cast<size_t>(units) * 4, kAlign); }
-size_t split_bytes(int64_t units, int G, int d) {
-  return static_cast<size_t>(units) * G * (d + 2) * sizeof(float) + kAlign;
+size_t cluster_partial_bytes(int64_t units, int G, int d) {
+  return static_cast<size_t>(units) * G * (d + 2) * sizeof(float);
 }
-size_t ws_bytes_for(int64_t units, int G, int d, int splits) {
+size_t ws_bytes_for(int64_t units, int G, int d, int nc) {
+  if (nc <= 1) return kAlign;
   return kAlign + counters_bytes(units) +
-         round_up(static_cast<size_t>(units) * splits * G * 2 * sizeof(float), kAlign) +
-         static_cast<size_t>(units) * splits * G * d * sizeof(float);
+         round_up(static_cast<size_t>(units) * nc * G * 2 * sizeof(float), kAlign) +
+         static_cast<size_t>(units) * nc * G * d * sizeof(float);
 }
 
-int64_t chunks_max_of(int T, int max_teams, int M, bool dense) {
-  const int64_t teams = dense ? max_teams : std::min(M, max_teams);
+int64_t chunks_max_of(int T, int max_teams, int M, int mode) {
+  if (mode == santa::kModeSample) return 0;
+  const int64_t teams = mode == santa::kModeDense ? max_teams : std::min(M, max_teams);
   return teams * (T / santa::kChunk);
 }
 
-// Splits needed so that no CTA owns more than kMaxChunksPerSplit chunks.
-int64_t min_splits_of(int64_t chunks_max) {
-  return ceil_div(chunks_max, santa::kMaxChunksPerSplit);
+int pow2_at_least(int64_t x) {
+  int c = 1;
+  while (c < x) c <<= 1;
+  return c;
 }
 
-// Resident attention CTAs per SM for a shape (cached per device and shape).
 int resident_ctas(bool bf16, int d, int G) {
   static std::mutex mu;
   static int cache[64][2][2][santa::kMaxGroup + 1] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  int& c = cache[dev][bf16 ? 1 : 0][d == 128 ? 1 : 0][G];
-  if (!c) c = std::max(1, santa::attend_resident_ctas(santa::AttendShape{bf16, d, G}));
+  int& c = cache[dev][bf16][d == 128][G];
+  if (!c) c = bf16 ? santa::decode_resident_bf16(d, G) : santa::decode_resident_f32(d, G);
   return c;
 }
 
-// Default split: one wave of resident CTAs over the whole job, i.e. each unit gets
-// floor(SMs * resident / units) splits (at least one, at most kMaxSplits).
-void default_split(int64_t units, int64_t chunks_max, int sms, int resident, int64_t* cps,
-                   int64_t* splits) {
-  const int64_t slots = std::max<int64_t>(1, static_cast<int64_t>(sms) * resident);
-  const int64_t per_unit = std::min<int64_t>(santa::kMaxSplits, std::max<int64_t>(1, slots / units));
-  *cps = std::max<int64_t>(ceil_div(chunks_max, per_unit), 1);
-  *cps = std::min<int64_t>(*cps, santa::kMaxChunksPerSplit);
-  *splits = ceil_div(chunks_max, *cps);
+// Clusters of `cl` CTAs the device can run at once (cached per device and shape).
+int max_clusters(bool bf16, int d, int G, int cl) {
+  static std::mutex mu;
+  static int cache[64][2][2][santa::kMaxGroup + 1][5] = {};  // 0 unknown, -1 none
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int li = 0;
+  while ((1 << li) < cl) ++li;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[dev][bf16][d == 128][G][li];
+  if (!c) {
+    const int n = bf16 ? santa::decode_max_clusters_bf16(d, G, cl)
+                       : santa::decode_max_clusters_f32(d, G, cl);
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
 }
 
 struct Plan {
-  int chunks_per_split = 1;
-  int splits = 1;
-  int cap = 0;
+  int cluster = 1;       // CL
+  int clusters = 1;      // NC
+  int tpc = 1;           // teams per CTA in the sampling phase
   uint32_t* counters = nullptr;
   float* part_ml = nullptr;
   float* part_acc = nullptr;
 };
 
-int make_plan(const santa_decode_args* a, bool dense, Plan* pl) {
+// Chooses CL and NC for a shape; nc_cap limits NC (the workspace's capacity).
+int choose(int dtype, int64_t units, int G, int d, int T, int max_teams, int M, int mode,
+           int64_t nc_cap, Plan* pl) {
+  const bool bf16 = dtype == SANTA_BF16;
+  const int sms = current_sms();
+  const int res = resident_ctas(bf16, d, G);
+  if (sms <= 0 || res <= 0) return SANTA_ERR_CUDA;
+  const int64_t slots = static_cast<int64_t>(sms) * res;
+  const int64_t spu = std::max<int64_t>(1, slots / units);
+  const bool sampling = mode == santa::kModeDecode || mode == santa::kModeSample;
+  const int64_t cmax = chunks_max_of(T, max_teams, M, mode);
+  // smallest cluster that keeps per-CTA tables in bounds
+  int64_t cl_min = 1;
+  if (sampling) cl_min = std::max<int64_t>(cl_min, ceil_div(max_teams, santa::kMaxTeamsPerCta));
+  const int64_t nc_limit = std::min<int64_t>(santa::kMaxClustersPerUnit, std::max<int64_t>(1, nc_cap));
+  cl_min = std::max<int64_t>(cl_min, ceil_div(cmax, santa::kMaxChunksPerSplit * nc_limit));
+  int cl_lo = pow2_at_least(cl_min);
+  if (cl_lo > santa::kMaxCluster) return SANTA_ERR_UNSUPPORTED;
+  int cl_start = 1;
+  while (cl_start * 2 <= std::min<int64_t>(spu, santa::kMaxCluster)) cl_start *= 2;
+  cl_start = std::max(cl_start, cl_lo);
+  // Cluster size: the largest power of two (<= units' share of one wave, <= 16) whose
+  // clusters can all be resident at once; failing that, the smallest allowed.  Clusters per
+  // unit: as few as keep every CTA's chunk table in bounds.  A dense step (no sampling to
+  // repeat per cluster) also takes more clusters when each CTA would otherwise stream more
+  // than 8 chunks and the extra clusters still fit the wave.
+  int cl = -1;
+  int64_t nc = 1;
+  for (int c = cl_start; c >= cl_lo; c >>= 1) {
+    const int maxc = max_clusters(bf16, d, G, c);
+    if (maxc <= 0) continue;
+    const int64_t nc_min = cmax > 0 ? ceil_div(cmax, static_cast<int64_t>(santa::kMaxChunksPerSplit) * c) : 1;
+    if (nc_min > nc_limit) continue;
+    int64_t n_c = nc_min;
+    if (mode == santa::kModeDense) {
+      const int64_t want = ceil_div(ceil_div(cmax, c), 8);
+      const int64_t room = std::max<int64_t>(1, maxc / units);
+      n_c = std::max(nc_min, std::min({want, room, nc_limit}));
+    }
+    cl = c;
+    nc = n_c;
+    if (units * n_c <= maxc) break;
+  }
+  if (cl < 0) return SANTA_ERR_UNSUPPORTED;
+  pl->cluster = cl;
+  pl->clusters = static_cast<int>(nc);
+  pl->tpc = static_cast<int>(std::max<int64_t>(1, ceil_div(max_teams, cl)));
+  return SANTA_OK;
+}
+
+int make_plan(const santa_decode_args* a, int mode, Plan* pl) {
   const int64_t units = static_cast<int64_t>(a->batch) * a->num_kv_heads;
   const int G = a->num_q_heads / a->num_kv_heads, d = a->head_dim;
-  if (!a->workspace) return SANTA_ERR_INVALID_ARG;
-  const uintptr_t raw = reinterpret_cast<uintptr_t>(a->workspace);
-  const uintptr_t base = round_up(raw, kAlign);
-  const size_t lead = base - raw;
-  const size_t fixed = lead + counters_bytes(units);
-  if (a->workspace_bytes < fixed + split_bytes(units, G, d)) return SANTA_ERR_INVALID_ARG;
-  int64_t cap = static_cast<int64_t>((a->workspace_bytes - fixed - kAlign) /
-                                     (static_cast<size_t>(units) * G * (d + 2) * sizeof(float)));
-  const int64_t cmax = chunks_max_of(a->team_size, a->max_teams, a->num_draws, dense);
-  cap = std::min<int64_t>({cap, cmax, static_cast<int64_t>(santa::kMaxSplits)});
-  if (cap < min_splits_of(cmax)) return SANTA_ERR_INVALID_ARG;
-  const int sms = current_sms();
-  if (sms <= 0) return SANTA_ERR_CUDA;
-  int64_t cps, splits;
-  default_split(units, cmax, sms, resident_ctas(a->dtype == SANTA_BF16, d, G), &cps, &splits);
-  if (splits > cap) {
-    cps = ceil_div(cmax, cap);
-    splits = ceil_div(cmax, cps);
+  // clusters per unit the workspace can hold
+  int64_t nc_cap = 1;
+  uintptr_t base = 0;
+  if (a->workspace && a->workspace_bytes > 0) {
+    const uintptr_t raw = reinterpret_cast<uintptr_t>(a->workspace);
+    base = round_up(raw, kAlign);
+    const size_t fixed = (base - raw) + counters_bytes(units) + kAlign;
+    if (a->workspace_bytes > fixed)
+      nc_cap = std::max<int64_t>(1, static_cast<int64_t>((a->workspace_bytes - fixed) /
+                                                         cluster_partial_bytes(units, G, d)));
   }
-  pl->chunks_per_split = static_cast<int>(cps);
-  pl->splits = static_cast<int>(splits);
-  pl->cap = static_cast<int>(cap);
-  unsigned char* b = reinterpret_cast<unsigned char*>(base);
-  pl->counters = reinterpret_cast<uint32_t*>(b);
-  b += counters_bytes(units);
-  pl->part_ml = reinterpret_cast<float*>(b);
-  b += round_up(static_cast<size_t>(units) * cap * G * 2 * sizeof(float), kAlign);
-  pl->part_acc = reinterpret_cast<float*>(b);
+  int rc = choose(a->dtype, units, G, d, a->team_size, a->max_teams, a->num_draws, mode, nc_cap,
+                  pl);
+  if (rc) return rc;
+  if (pl->clusters > 1) {
+    if (!base) return SANTA_ERR_INVALID_ARG;
+    unsigned char* b = reinterpret_cast<unsigned char*>(base);
+    pl->counters = reinterpret_cast<uint32_t*>(b);
+    b += counters_bytes(units);
+    pl->part_ml = reinterpret_cast<float*>(b);
+    b += round_up(static_cast<size_t>(units) * pl->clusters * G * 2 * sizeof(float), kAlign);
+    pl->part_acc = reinterpret_cast<float*>(b);
+  }
   return SANTA_OK;
 }
 
 size_t default_ws_bytes(int dtype, int batch, int hq, int hkv, int d, int T, int max_teams,
-                        int M, bool dense) {
+                        int M, int mode) {
   if (check_shape(dtype, batch, hq, hkv, d, T, max_teams)) return 0;
-  if (!dense && (M < 1 || M > kMaxDraws)) return 0;
+  if (mode != santa::kModeDense && (M < 1 || M > kMaxDraws)) return 0;
+  Plan pl;
   const int64_t units = static_cast<int64_t>(batch) * hkv;
-  const int G = hq / hkv;
-  const int sms = current_sms();
-  if (sms <= 0) return 0;
-  const int64_t cmax = chunks_max_of(T, max_teams, M, dense);
-  int64_t cps, splits;
-  default_split(units, cmax, sms, resident_ctas(dtype == SANTA_BF16, d, G), &cps, &splits);
-  return ws_bytes_for(units, G, d, static_cast<int>(splits));
+  if (choose(dtype, units, hq / hkv, d, T, max_teams, M, mode, santa::kMaxClustersPerUnit, &pl))
+    return 0;
+  return ws_bytes_for(units, hq / hkv, d, pl.clusters);
 }
 
-// Cluster size of the sampling kernel: enough CTAs that each scores about 32 teams, at most
-// 8 (so at most 2048 teams per CTA for the longest supported sequence).
-int sample_cluster(int max_teams) {
-  int cl = 1;
-  while (cl < 8 && cl * 32 < max_teams) cl <<= 1;
-  return cl;
-}
-
-int do_sample(const santa_decode_args* a, cudaStream_t stream) {
+int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   int rc = check_inputs(a);
   if (rc) return rc;
-  if ((rc = check_draws(a))) return rc;
-  if (!a->reps || !aligned(a->reps, 16) || !a->draw_ids || !aligned(a->draw_ids, 4))
-    return SANTA_ERR_INVALID_ARG;
-  if (a->team_probs && !aligned(a->team_probs, 4)) return SANTA_ERR_INVALID_ARG;
-  uint32_t* counters = nullptr;
-  if (a->workspace) {
-    Plan pl;
-    if ((rc = make_plan(a, false, &pl))) return rc;
-    counters = pl.counters;
+  const bool sampling = mode == santa::kModeDecode || mode == santa::kModeSample;
+  if (mode != santa::kModeDense && (rc = check_draws(a))) return rc;
+  if (sampling) {
+    if (!a->reps || !aligned(a->reps, 16) || !a->draw_ids || !aligned(a->draw_ids, 4))
+      return SANTA_ERR_INVALID_ARG;
+    if (a->team_probs && !aligned(a->team_probs, 4)) return SANTA_ERR_INVALID_ARG;
   }
-  const int cl = sample_cluster(a->max_teams);
-  SampleParams p;
+  if (mode != santa::kModeSample && (!a->out || !aligned(a->out, 16)))
+    return SANTA_ERR_INVALID_ARG;
+  Plan pl;
+  if ((rc = make_plan(a, mode, &pl))) return rc;
+  DecodeParams p = {};
   p.q = a->q;
-  p.reps = a->reps;
+  p.k_pool = a->k_pool;
+  p.v_pool = a->v_pool;
+  p.reps = sampling ? a->reps : nullptr;
   p.page_table = a->page_table;
   p.seq_lens = a->seq_lens;
-  p.is_bf16 = a->dtype == SANTA_BF16;
   p.batch = a->batch;
   p.num_q_heads = a->num_q_heads;
   p.num_kv_heads = a->num_kv_heads;
-  p.group = a->num_q_heads / a->num_kv_heads;
   p.team_size = a->team_size;
   p.max_teams = a->max_teams;
-  p.num_draws = a->num_draws;
+  p.num_draws = mode == santa::kModeDense ? 1 : a->num_draws;
   p.num_pages = a->num_pages;
   p.seed = a->seed;
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(a->head_dim)));
-  p.teams_per_cta = static_cast<int>(ceil_div(a->max_teams, cl));
+  p.scale_log2 =
+      static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a->head_dim)));
+  p.mode = mode;
+  p.teams_per_cta = pl.tpc;
+  p.clusters_per_unit = pl.clusters;
+  p.out = a->out;
   p.draw_ids = a->draw_ids;
   p.sel_ids = a->sel_ids;
   p.sel_count = a->sel_count;
   p.pi = a->pi;
-  p.team_probs = a->team_probs;
-  p.counters = counters;
-  p.status = a->device_status;
-  return map_cuda(santa::launch_sample(p, a->head_dim, cl, stream));
-}
-
-int do_attend(const santa_decode_args* a, bool dense, bool programmatic, cudaStream_t stream) {
-  int rc = check_inputs(a);
-  if (rc) return rc;
-  if (!dense && (rc = check_draws(a))) return rc;
-  if (!a->out || !aligned(a->out, 16)) return SANTA_ERR_INVALID_ARG;
-  Plan pl;
-  if ((rc = make_plan(a, dense, &pl))) return rc;
-  AttendParams p;
-  p.q = a->q;
-  p.k_pool = a->k_pool;
-  p.v_pool = a->v_pool;
-  p.page_table = a->page_table;
-  p.seq_lens = a->seq_lens;
-  p.sel_ids = dense ? nullptr : a->sel_ids;
-  p.sel_count = dense ? nullptr : a->sel_count;
-  p.pi = dense ? nullptr : a->pi;
-  p.batch = a->batch;
-  p.num_q_heads = a->num_q_heads;
-  p.num_kv_heads = a->num_kv_heads;
-  p.team_size = a->team_size;
-  p.max_teams = a->max_teams;
-  p.num_draws = dense ? 0 : a->num_draws;
-  p.num_pages = a->num_pages;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(a->head_dim)));
-  p.dense = dense ? 1 : 0;
-  p.chunks_per_split = pl.chunks_per_split;
-  p.max_splits = pl.cap;
+  p.team_probs = sampling ? a->team_probs : nullptr;
   p.part_ml = pl.part_ml;
   p.part_acc = pl.part_acc;
   p.counters = pl.counters;
-  p.out = a->out;
   p.status = a->device_status;
-  AttendShape s{a->dtype == SANTA_BF16, a->head_dim, a->num_q_heads / a->num_kv_heads};
-  const dim3 grid(pl.splits, a->num_kv_heads, a->batch);
-  return map_cuda(santa::launch_attend(p, s, grid, programmatic, stream));
+  const dim3 grid(pl.cluster * pl.clusters, a->num_kv_heads, a->batch);
+  const int G = a->num_q_heads / a->num_kv_heads;
+  const cudaError_t e =
+      a->dtype == SANTA_BF16
+          ? santa::decode_launch_bf16(p, a->head_dim, G, grid, pl.cluster, stream)
+          : santa::decode_launch_f32(p, a->head_dim, G, grid, pl.cluster, stream);
+  return map_cuda(e);
 }
 
 int do_reps(const void* k_pool, int dtype, int64_t num_pages, int hkv, int T, int d,
@@ -295,26 +316,8 @@ int do_reps(const void* k_pool, int dtype, int64_t num_pages, int hkv, int T, in
 
 }  // namespace
 
-namespace santa {
-
-cudaError_t launch_attend(const AttendParams& p, const AttendShape& s, dim3 grid,
-                          bool programmatic, cudaStream_t stream) {
-  return s.is_bf16 ? launch_attend_bf16(p, s.head_dim, s.group, grid, programmatic, stream)
-                   : launch_attend_f32(p, s.head_dim, s.group, grid, programmatic, stream);
-}
-
-int attend_resident_ctas(const AttendShape& s) {
-  return s.is_bf16 ? attend_resident_ctas_bf16(s.head_dim, s.group)
-                   : attend_resident_ctas_f32(s.head_dim, s.group);
-}
-
-size_t attend_smem_bytes(const AttendShape& s) {
-  return s.is_bf16 ? attend_smem_bytes_bf16(s.head_dim, s.group)
-                   : attend_smem_bytes_f32(s.head_dim, s.group);
-}
-
-}  // namespace santa
-
+// Only the C ABI is exported (the library is built with -fvisibility=hidden).
+#pragma GCC visibility push(default)
 extern "C" {
 
 int santa_abi_version(void) { return SANTA_ABI_VERSION; }
@@ -350,7 +353,7 @@ int santa_update_reps(const void* k_pool, int dtype, int64_t num_pages, int num_
 size_t santa_decode_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
                                     int head_dim, int team_size, int max_teams, int num_draws) {
   return default_ws_bytes(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size,
-                          max_teams, num_draws, false);
+                          max_teams, num_draws, santa::kModeDecode);
 }
 
 size_t santa_decode_workspace_min_bytes(int batch, int num_q_heads, int num_kv_heads,
@@ -359,36 +362,53 @@ size_t santa_decode_workspace_min_bytes(int batch, int num_q_heads, int num_kv_h
   if (check_shape(SANTA_F32, batch, num_q_heads, num_kv_heads, head_dim, team_size, max_teams))
     return 0;
   if (num_draws < 1 || num_draws > kMaxDraws) return 0;
+  // with the largest cluster, a unit needs ceil(chunks / (16 * kMaxChunksPerSplit)) clusters
   const int64_t units = static_cast<int64_t>(batch) * num_kv_heads;
-  const int64_t splits = min_splits_of(chunks_max_of(team_size, max_teams, num_draws, false));
-  return kAlign + counters_bytes(units) +
-         static_cast<size_t>(splits) * (split_bytes(units, num_q_heads / num_kv_heads, head_dim) -
-                                        kAlign) + kAlign;
+  const int64_t cmax = chunks_max_of(team_size, max_teams, num_draws, santa::kModeDecode);
+  const int64_t nc = ceil_div(cmax, static_cast<int64_t>(santa::kMaxCluster) *
+                                        santa::kMaxChunksPerSplit);
+  return ws_bytes_for(units, num_q_heads / num_kv_heads, head_dim, static_cast<int>(nc));
 }
 
 size_t santa_dense_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
                                    int head_dim, int team_size, int max_teams) {
   return default_ws_bytes(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size,
-                          max_teams, 1, true);
+                          max_teams, 1, santa::kModeDense);
+}
+
+int santa_decode_plan(const santa_decode_args* a, int which, int32_t* out) {
+  if (!a || !out || which < santa::kModeDecode || which > santa::kModeDense)
+    return SANTA_ERR_INVALID_ARG;
+  int rc = check_shape(a->dtype, a->batch, a->num_q_heads, a->num_kv_heads, a->head_dim,
+                       a->team_size, a->max_teams);
+  if (rc) return rc;
+  if (which != santa::kModeDense && (a->num_draws < 1 || a->num_draws > kMaxDraws))
+    return SANTA_ERR_UNSUPPORTED;
+  Plan pl;
+  if ((rc = make_plan(a, which, &pl))) return rc;
+  out[0] = pl.cluster;
+  out[1] = pl.clusters;
+  out[2] = pl.tpc;
+  out[3] = max_clusters(a->dtype == SANTA_BF16, a->head_dim, a->num_q_heads / a->num_kv_heads,
+                        pl.cluster);
+  return SANTA_OK;
 }
 
 int santa_sample(const santa_decode_args* a, void* stream) {
-  return do_sample(a, static_cast<cudaStream_t>(stream));
+  return launch(a, santa::kModeSample, static_cast<cudaStream_t>(stream));
 }
 
 int santa_attend(const santa_decode_args* a, void* stream) {
-  return do_attend(a, false, false, static_cast<cudaStream_t>(stream));
+  return launch(a, santa::kModeAttend, static_cast<cudaStream_t>(stream));
 }
 
 int santa_decode(const santa_decode_args* a, void* stream) {
-  if (!a || !a->workspace) return SANTA_ERR_INVALID_ARG;
-  int rc = do_sample(a, static_cast<cudaStream_t>(stream));
-  if (rc) return rc;
-  return do_attend(a, false, true, static_cast<cudaStream_t>(stream));
+  return launch(a, santa::kModeDecode, static_cast<cudaStream_t>(stream));
 }
 
 int santa_dense_decode(const santa_decode_args* a, void* stream) {
-  return do_attend(a, true, false, static_cast<cudaStream_t>(stream));
+  return launch(a, santa::kModeDense, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
+#pragma GCC visibility pop

@@ -39,6 +39,8 @@ void* scratch_address() {
 
 }  // namespace
 
+// Only the C ABI is exported (the library is built with -fvisibility=hidden).
+#pragma GCC visibility push(default)
 extern "C" int santa_decode_noalloc(const santa_decode_args* a, void* stream) {
   if (!a) return SANTA_ERR_INVALID_ARG;
   const size_t need = santa_decode_workspace_min_bytes(a->batch, a->num_q_heads,
@@ -56,3 +58,4 @@ extern "C" int santa_decode_noalloc(const santa_decode_args* a, void* stream) {
 }
 
 extern "C" size_t santa_noalloc_scratch_bytes(void) { return kStaticScratchBytes; }
+#pragma GCC visibility pop

@@ -66,17 +66,15 @@ def test_sample_rejects_bad_arguments_on_host(lib, field, value, expect):
     assert lib.santa_sample(ctypes.byref(a), None) == expect
 
 
-def test_null_args_and_missing_workspace(lib):
-    for fn in ("santa_sample", "santa_attend", "santa_decode", "santa_dense_decode"):
+def test_null_args(lib):
+    for fn in ("santa_sample", "santa_attend", "santa_decode", "santa_dense_decode",
+               "santa_decode_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
         assert getattr(lib, fn)(None, None) == INVALID
     a = valid_args()
-    a.workspace = None
+    a.out = 0
     assert lib.santa_attend(ctypes.byref(a), None) == INVALID
     assert lib.santa_decode(ctypes.byref(a), None) == INVALID
-    a = valid_args()
-    a.workspace, a.workspace_bytes = 0x20000, 16    # far too small
-    assert lib.santa_attend(ctypes.byref(a), None) == INVALID
 
 
 def test_reps_reject_bad_arguments_on_host(lib):
@@ -94,9 +92,10 @@ def test_minimum_workspace_size(lib):
     f = lib.santa_decode_workspace_min_bytes
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int] * 7
-    # 256 alignment slack + counters (rounded to 256) + one split (<= 256 chunks of 64
-    # tokens each): units*G*(d+2)*4 + 256
-    assert f(1, 28, 4, 128, 128, 256, 31) == 256 + 256 + 4 * 7 * 130 * 4 + 256
-    # 4096 draws over 16384 teams of 128 tokens: 8192 chunks -> 32 splits
-    assert f(1, 28, 4, 128, 128, 16384, 4096) == 256 + 256 + 32 * 4 * 7 * 130 * 4 + 256
+    # a unit needs scratch only when it spans several clusters: with 16-CTA clusters of at
+    # most 256 chunks (64 tokens) each, 31 draws over 256 teams fit one cluster
+    assert f(1, 28, 4, 128, 128, 256, 31) == 256
+    # 4096 draws of 128-token teams: 8192 chunks -> 2 clusters; 256 slack + counters (256)
+    # + (m, l) [4][2][7][2] fp32 rounded to 256 + acc [4][2][7][128] fp32
+    assert f(1, 28, 4, 128, 128, 16384, 4096) == 256 + 256 + 512 + 4 * 2 * 7 * 128 * 4
     assert f(1, 30, 4, 128, 128, 256, 31) == 0

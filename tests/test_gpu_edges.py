@@ -86,25 +86,29 @@ def test_peaked_distribution_with_underflow():
 
 
 def test_workspace_of_minimum_size():
-    """The smallest workspace the library accepts (one split per unit) gives the same
-    result as the default one."""
-    wl = W.generate("qwen7b_32k_b8_m64", batch=2, seq_len=5000)
-    dw = DeviceWorkload(wl)
-    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
-    cfg = wl.cfg
-    full = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
-                              cfg.draws, 3)
-    mt = dw.page_table.shape[1]
-    small = DecodeBuffers.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads,
-                                   cfg.head_dim, cfg.team_size, mt, cfg.draws)
-    small.workspace = torch.zeros(santa.santa_decode_workspace_min_bytes(
-        cfg.batch, cfg.q_heads, cfg.kv_heads, cfg.head_dim, cfg.team_size, mt, cfg.draws),
-        dtype=torch.uint8, device="cuda")
-    santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
-                       cfg.draws, 3, bufs=small)
-    torch.cuda.synchronize()
-    assert torch.equal(full.sel_ids, small.sel_ids)
-    assert (full.out - small.out).abs().max().item() <= 1e-5
+    """The smallest workspace the library accepts gives the same sampled sets and the same
+    output (to rounding) as the default one, also for a unit whose work spans several
+    clusters (4096 draws over 4096 teams)."""
+    for name, over in [("qwen7b_32k_b8_m64", dict(batch=2, seq_len=5000)),
+                       ("tiny_f32", dict(seq_len=4096 * 128, team_size=128, draws=4096))]:
+        wl = W.generate(name, **over)
+        dw = DeviceWorkload(wl)
+        reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+        cfg = wl.cfg
+        full = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table,
+                                  dw.seq_lens, cfg.draws, 3)
+        mt = dw.page_table.shape[1]
+        small = DecodeBuffers.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads,
+                                       cfg.head_dim, cfg.team_size, mt, cfg.draws)
+        small.workspace = torch.zeros(santa.santa_decode_workspace_min_bytes(
+            cfg.batch, cfg.q_heads, cfg.kv_heads, cfg.head_dim, cfg.team_size, mt, cfg.draws),
+            dtype=torch.uint8, device="cuda")
+        santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
+                           cfg.draws, 3, bufs=small)
+        torch.cuda.synchronize()
+        assert full.status() == 0 and small.status() == 0
+        assert torch.equal(full.sel_ids, small.sel_ids)
+        assert (full.out - small.out).abs().max().item() <= 1e-5
 
 
 def test_repeated_calls_are_deterministic():

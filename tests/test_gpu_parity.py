@@ -34,7 +34,23 @@ SMALL = {
                          q_heads=8, kv_heads=2, draws=20),
     "f32_d128_g8": dict(cfg="tiny_f32", head_dim=128, team_size=128, seq_len=5000,
                         q_heads=16, kv_heads=2, draws=12),
+    # one long sequence, one KV head: dense work spans several clusters
+    "long_b1_multicluster": dict(cfg="long_128k_b4_m64", batch=1, q_heads=7, kv_heads=1,
+                                 seq_len=40000, draws=600, num_pages=0),
+    # 4096 draws over 4096 teams: more chunks than one cluster's tables hold, so the sampled
+    # step itself spans two clusters (partials through the workspace)
+    "f32_b1_two_clusters": dict(cfg="tiny_f32", seq_len=4096 * 128, team_size=128,
+                                draws=4096),
 }
+
+
+def test_multicluster_cases_take_the_multicluster_path():
+    for name, which in [("long_b1_multicluster", "dense"), ("f32_b1_two_clusters", "decode"),
+                        ("f32_b1_two_clusters", "attend")]:
+        wl = make(SMALL[name])
+        dw = DeviceWorkload(wl)
+        plan = santa.santa_decode_plan(dw.q, dw.k_pool, dw.page_table, wl.cfg.draws, which)
+        assert plan["clusters_per_unit"] >= 2, (name, which, plan)
 
 
 def make(spec, **extra):

@@ -18,11 +18,18 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("name,overrides", [
     ("qwen7b_32k_b8_m64", dict(batch=3, seq_len=9000)),
     ("tiny_f32", {}),
+    # 4096 draws over 4096 teams: the unit spans two clusters, whose partials go through
+    # the scratch
+    ("tiny_f32", dict(seq_len=4096 * 128, team_size=128, draws=4096)),
 ])
 def test_noalloc_matches_decode_on_two_calls(name, overrides):
     wl = W.generate(name, **overrides)
     cfg = wl.cfg
     dw = DeviceWorkload(wl)
+    if cfg.draws == 4096:
+        plan = santa.santa_decode_plan(dw.q, dw.k_pool, dw.page_table, cfg.draws, "decode",
+                                       workspace_bytes=santa.santa_noalloc_scratch_bytes())
+        assert plan["clusters_per_unit"] >= 2, plan
     reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
     ref = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
                              cfg.draws, 77)
@@ -45,17 +52,17 @@ def test_noalloc_matches_decode_on_two_calls(name, overrides):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
+    """512 units of 4096 draws over 4096 teams need two clusters' partials per unit, more
+    than the built-in scratch holds: the call is refused before anything runs."""
+    B, Hq, Hkv, d, T, teams, M = 64, 64, 8, 128, 128, 4096, 4096
     cap = santa.santa_noalloc_scratch_bytes()
-    need = santa.santa_decode_workspace_min_bytes(512, 2, 1, 64, 64, 16384, 4096)
-    assert need > cap
-    wl = W.generate("tiny_f32")
-    dw = DeviceWorkload(wl)
-    reps = santa.santa_build_reps(dw.k_pool)
-    B = 512
-    q = dw.q.expand(B, -1, -1).contiguous()
-    pt = dw.page_table.expand(B, -1).contiguous()
-    pt = torch.nn.functional.pad(pt, (0, 16384 - pt.shape[1]))
-    lens = dw.seq_lens.expand(B).contiguous()
-    bufs = DecodeBuffers.allocate(q.dtype, B, 2, 1, 64, 64, 16384, 4096)
+    assert santa.santa_decode_workspace_min_bytes(B, Hq, Hkv, d, T, teams, M) > cap
+    dev = "cuda"
+    q = torch.zeros((B, Hq, d), dtype=torch.bfloat16, device=dev)
+    k = torch.zeros((4, Hkv, T, d), dtype=torch.bfloat16, device=dev)
+    reps = torch.zeros((4, Hkv, d), dtype=torch.float32, device=dev)
+    pt = torch.zeros((B, teams), dtype=torch.int32, device=dev)
+    lens = torch.full((B,), T, dtype=torch.int32, device=dev)
+    bufs = DecodeBuffers.allocate(q.dtype, B, Hq, Hkv, d, T, teams, M)
     with pytest.raises(santa.SantaError, match="scratch"):
-        santa.santa_decode_noalloc(q, dw.k_pool, dw.v_pool, reps, pt, lens, 4096, 1, bufs)
+        santa.santa_decode_noalloc(q, k, k, reps, pt, lens, M, 1, bufs)
