@@ -81,6 +81,8 @@ typedef enum santa_dtype { SANTA_F32 = 0, SANTA_BF16 = 1 } santa_dtype;
 #define SANTA_DEV_BAD_SEQLEN 2u  /* seq_len < 1 or seq_len > max_teams * team_size */
 #define SANTA_DEV_BAD_SEL 4u     /* santa_attend given a sel_ids/sel_count/pi entry out of range */
 #define SANTA_DEV_TIMEOUT 8u     /* a bounded wait on an asynchronous copy gave up (2 s) */
+#define SANTA_DEV_LAYOUT 16u     /* shared memory not 1 KiB-aligned for the swizzled tile copies;
+                                   the kernel returned without writing outputs */
 
 /* Returns SANTA_ABI_VERSION of the loaded library. */
 int santa_abi_version(void);

@@ -83,16 +83,19 @@ struct DecodeTraits {
   static constexpr int kEplS = D / 16;
   static constexpr int kEplV = D / 32;
   static constexpr int kRing = kStages * kStageBytes;
-  // phase A scratch inside the ring: cdf (uint64) [tpc], es [8][tpc], ps [tpc], flag [tpc],
-  // then a buffer of representative rows (fp32 [rows][D]) for as many rows as fit
-  static constexpr size_t sample_scratch(int tpc) {
-    return sizeof(unsigned long long) * tpc + sizeof(float) * kMaxGroup * tpc +
-           sizeof(float) * tpc + sizeof(int) * tpc;
+  // phase A scratch inside the ring, for `cap` teams: cdf (uint64), es [8][cap], ps, flag,
+  // the drawn-team list (local path), then rows of representatives (fp32 [rows][D])
+  static constexpr size_t sample_scratch(int cap) {   // rounded up to 128 bytes (the rows
+    return ((sizeof(unsigned long long) + sizeof(float) * kMaxGroup + sizeof(float) +  // take
+             sizeof(int) + sizeof(ListEntry)) * static_cast<size_t>(cap) + 127) /  // 16-byte
+           128 * 128;                                                        // copies)
   }
-  static constexpr int rep_rows(int tpc) {
-    return static_cast<int>((static_cast<size_t>(kRing) - sample_scratch(tpc)) / (D * 4));
+  static constexpr int rep_rows(int cap) {
+    return static_cast<int>((static_cast<size_t>(kRing) - sample_scratch(cap)) / (D * 4));
   }
   static_assert(rep_rows(kMaxTeamsPerCta) >= 32, "representative buffer must hold 32 rows");
+  static_assert(sizeof(ListEntry) * kMaxTeamsPerCta >= sizeof(float) * kPubScores,
+                "the list region must hold the published scores");
   // phase D: warp merge buffer [8][G][D] + m, l [8][8], then the CTA partial [G][D] + m, l
   static constexpr int kMergeFloats = kWarps * G * D + 2 * kWarps * kMaxGroup;
   static constexpr int kPartialOff = kMergeFloats;                    // in floats
@@ -214,11 +217,67 @@ __device__ __forceinline__ V block_inclusive_scan(V v, V* warp_tot, V& block_tot
   return res;
 }
 
+// Scores s_{g,j} = q_g . rep_j / sqrt(d) of teams [t0, t0 + cnt) of unit (b, h), written
+// to es[g * stride + j] (j relative to t0); flag[j] = -2 marks a team whose page id is out
+// of range (score -inf, status bit), else 0.  The fp32 representative rows are staged in
+// shared memory with 16-byte asynchronous copies issued by every thread (one round trip per
+// batch of `rows_cap` rows); 16 lanes score one team (d/16 elements each, q in registers in
+// the same layout) and an 8-shuffle reduce-scatter leaves lane l with head (l >> 1) & 7.
+template <int D, int G>
+__device__ __forceinline__ void score_teams(const DecodeParams& p, int b, int h, int t0, int cnt,
+                                            const float (&qs)[G][D / 16], float* rows,
+                                            int rows_cap, float* es, int stride, int* flag) {
+  constexpr int kQuads = D / 4;                    // 16-byte pieces of a row
+  constexpr float kNegInf = -INFINITY;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, lane16 = lane & 15;
+  const int hh = (lane >> 1) & 7;
+  for (int j0 = 0; j0 < cnt; j0 += rows_cap) {
+    const int bc = min(rows_cap, cnt - j0);
+    for (int c = tid; c < bc * kQuads; c += 256) {
+      const int j = c / kQuads, k = c - j * kQuads;
+      const int64_t page = p.page_table[static_cast<int64_t>(b) * p.max_teams + t0 + j0 + j];
+      const bool ok = page >= 0 && page < p.num_pages;
+      if (k == 0) {
+        flag[j0 + j] = ok ? 0 : -2;
+        if (!ok) set_status(p.status, SANTA_DEV_BAD_PAGE);
+      }
+      cp_async16(rows + static_cast<size_t>(j) * D + 4 * k,
+                 p.reps + ((ok ? page : 0) * p.num_kv_heads + h) * D + 4 * k);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    for (int jj = 2 * warp; jj < bc; jj += 16) {
+      const int j = jj + (lane >> 4);
+      float x[D / 16];
+      if (j < bc) {
+        load_score_row<false, D>(reinterpret_cast<const unsigned char*>(rows + static_cast<size_t>(j) * D),
+                                 lane16, x);
+      } else {
+#pragma unroll
+        for (int e = 0; e < D / 16; ++e) x[e] = 0.f;
+      }
+      float part[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        part[g] = 0.f;
+        if (g < G) {
+#pragma unroll
+          for (int e = 0; e < D / 16; ++e) part[g] = fmaf(qs[g][e], x[e], part[g]);
+        }
+      }
+      const float sum = reduce_scatter8(part, lane);
+      if (j < bc && !(lane & 1) && hh < G)
+        es[hh * stride + j0 + j] = flag[j0 + j] == 0 ? sum * p.scale : kNegInf;
+    }
+    __syncthreads();                               // rows may be refilled
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <bool BF16, int D, int G>
 __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
-    decode_kernel(const DecodeParams p) {
+    decode_kernel(const __grid_constant__ DecodeParams p) {
   using Tr = DecodeTraits<BF16, D, G>;
   constexpr int S = Tr::kStages;
   constexpr float kNegInf = -INFINITY;
@@ -236,7 +295,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
   const bool attending = mode != kModeSample;
   const bool writer = cidx == 0;          // the cluster that writes the sampling outputs
 
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];  // 128-byte swizzle atoms: 1 KiB
   ListEntry* list = reinterpret_cast<ListEntry*>(smem + Tr::kListOff);
   ChunkMeta* table = reinterpret_cast<ChunkMeta*>(smem + Tr::kTableOff);
   float* prow = reinterpret_cast<float*>(smem + Tr::kPOff);
@@ -250,7 +309,14 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
   __shared__ int s_base[17];
   __shared__ unsigned long long s_off, s_Z;
   __shared__ int s_abort, s_last;
-  __shared__ __align__(8) uint64_t s_rbar;
+  if constexpr (BF16) {
+    // The 128-byte-swizzled tile copies and the fragment addressing below both assume
+    // 1 KiB-aligned stages; the layout is the same for every CTA, so all leave together.
+    if (attending && (smem_u32(smem) & 1023u) != 0) {
+      if (tid == 0 && rank == 0 && cidx == 0) set_status(p.status, SANTA_DEV_LAYOUT);
+      return;
+    }
+  }
 
   // ---- per-unit lengths
   const int L = p.seq_lens[b];
@@ -262,7 +328,6 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
-    mbar_init(&s_rbar, 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -270,232 +335,347 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
 
   // ================================================================ phase A: sampling
   int total_sel = 0;                      // |S| of the unit
+  // Exchange path: each CTA scores its slice of the teams and publishes the raw scores in
+  // its list region; after one cluster barrier every CTA reads all scores (one parallel
+  // DSMEM read) and samples the whole unit locally, so all CTAs hold the same S without
+  // further exchange.  Shapes whose slice scores do not fit the region use the
+  // distributed path (softmax statistics, CDF totals and counts exchanged in three rounds).
+  const int per = (n + CL - 1) / CL;
+  const bool local = G * per <= kPubScores && n <= kMaxTeamsPerCta;
+  ListEntry* llist = nullptr;             // local sampling: the drawn teams, in slot order
   if (sampling) {
-    const int tpc = p.teams_per_cta;
-    unsigned long long* cdf = reinterpret_cast<unsigned long long*>(smem);   // [tpc]
-    float* es = reinterpret_cast<float*>(cdf + tpc);                 // [8][tpc] scores, exps
-    float* ps = es + kMaxGroup * tpc;                                // [tpc] team probability
-    int* flag = reinterpret_cast<int*>(ps + tpc);                    // [tpc] drawn / slot
-    float* rows = reinterpret_cast<float*>(smem + Tr::sample_scratch(tpc));  // rep rows
-    const int max_rows = Tr::rep_rows(tpc);
-    const int per = (n + CL - 1) / CL;
-    const int lo = min(rank * per, n);
-    const int nl = min(lo + per, n) - lo;
-    constexpr int E = D / 32;
-
-    // q of the group in registers, lane l holding d-elements [l*E, (l+1)*E)
-    float qv[G][E];
+    const int cap = local ? max(n, 1) : p.teams_per_cta;
+    unsigned long long* cdf = reinterpret_cast<unsigned long long*>(smem);   // [cap]
+    float* es = reinterpret_cast<float*>(cdf + cap);                 // [8][cap] scores, exps
+    float* ps = es + kMaxGroup * cap;                                // [cap] team probability
+    int* flag = reinterpret_cast<int*>(ps + cap);                    // [cap] drawn / slot
+    llist = reinterpret_cast<ListEntry*>(flag + cap);                // [cap]
+    float* rows = reinterpret_cast<float*>(smem + Tr::sample_scratch(cap));
+    const int rows_cap = Tr::rep_rows(cap);
+    float* pub_scores = reinterpret_cast<float*>(list);              // [G][per], published
+    int lo = min(rank * per, n);
+    int nl = min(lo + per, n) - lo;
+    // q of the group in registers, in the fp32 score layout
+    float qs[G][Tr::kEplS];
     {
-      const int64_t qbase = (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D + lane * E;
+      const int64_t qbase = (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D;
 #pragma unroll
       for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-          qv[g][e] = BF16 ? bf16_to_f32(static_cast<const uint16_t*>(p.q)[qbase + g * D + e])
-                          : static_cast<const float*>(p.q)[qbase + g * D + e];
+        for (int e = 0; e < Tr::kEplS; ++e) {
+          const int64_t idx = qbase + g * D + score_elem<false, D>(lane16, e);
+          qs[g][e] = BF16 ? bf16_to_f32(static_cast<const uint16_t*>(p.q)[idx])
+                          : static_cast<const float*>(p.q)[idx];
+        }
     }
-    for (int j = tid; j < nl; j += Tr::kThreads) flag[j] = 0;
-
-    // scores, in batches of representative rows staged by bulk copies (one round trip each)
-    uint32_t rphase = 0;
-    for (int j0 = 0; j0 < nl; j0 += max_rows) {
-      const int cnt = min(max_rows, nl - j0);
-      if (tid == 0) mbar_arrive_expect_tx(&s_rbar, static_cast<uint32_t>(cnt) * D * 4);
+    if (local) {
+      score_teams<D, G>(p, b, h, lo, nl, qs, rows, rows_cap, pub_scores, per, flag);
+      cluster.sync();                                                // barrier S1
+      // all peers' published scores [G][per] into es [G][cap]: 16-byte DSMEM reads when the
+      // slice length allows, one parallel round trip
+      if ((per & 3) == 0) {
+        const int q4 = G * per / 4;                                  // float4 per peer
+        for (int i = tid; i < CL * q4; i += Tr::kThreads) {
+          const int r = i / q4, k = (i - r * q4) * 4;
+          const int g = k / per, jj = k - g * per, j = r * per + jj;
+          const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(pub_scores, r) + k);
+          float* dst = es + g * cap + j;
+          if (j + 3 < n) {
+            dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+          } else {
+            if (j < n) dst[0] = v.x;
+            if (j + 1 < n) dst[1] = v.y;
+            if (j + 2 < n) dst[2] = v.z;
+          }
+        }
+      } else {
+        for (int i = tid; i < G * n; i += Tr::kThreads) {
+          const int g = i / n, j = i - g * n;
+          const int r = j / per;
+          es[g * cap + j] = cluster.map_shared_rank(pub_scores, r)[g * per + (j - r * per)];
+        }
+      }
       __syncthreads();
-      for (int j = tid; j < cnt; j += Tr::kThreads) {
-        int64_t page = p.page_table[static_cast<int64_t>(b) * p.max_teams + lo + j0 + j];
-        const bool ok = page >= 0 && page < p.num_pages;
-        if (!ok) set_status(p.status, SANTA_DEV_BAD_PAGE);
-        flag[j0 + j] = ok ? 0 : -2;                  // -2: unusable team
-        bulk_g2s(rows + static_cast<size_t>(j) * D, p.reps + ((ok ? page : 0) * p.num_kv_heads + h) * D,
-                 D * 4, &s_rbar);
-      }
-      if (!mbar_wait(&s_rbar, rphase)) set_status(p.status, SANTA_DEV_TIMEOUT);
-      rphase ^= 1u;
-      for (int j = warp; j < cnt; j += Tr::kWarps) {
-        const float* rr = rows + static_cast<size_t>(j) * D + lane * E;
-        float rv[E];
-        if constexpr (E == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(rr);
-          rv[0] = v.x; rv[1] = v.y; rv[2] = v.z; rv[3] = v.w;
-        } else {
-          const float2 v = *reinterpret_cast<const float2*>(rr);
-          rv[0] = v.x; rv[1] = v.y;
+      // per-head max and sum of exp over all n teams: one warp per head
+      if (warp < G) {
+        float m = kNegInf;
+        for (int j = lane; j < n; j += 32) m = fmaxf(m, es[warp * cap + j]);
+        m = warp_max(m);
+        float z = 0.f;
+        if (m != kNegInf)
+          for (int j = lane; j < n; j += 32) {
+            const float sc = es[warp * cap + j];
+            z += sc == kNegInf ? 0.f : expf(sc - m);
+          }
+        z = warp_sum(z);
+        if (lane == 0) {
+          s_gm[warp] = m;
+          s_gz[warp] = z > 0.f ? 1.f / z : 0.f;                       // reciprocal
         }
-        const bool ok = flag[j0 + j] == 0;
+      }
+      __syncthreads();
+      // p_j = (1/G) sum_g exp(s_gj - m_g) / z_g, round(p_j 2^62) and the exact integer CDF,
+      // 256 teams per block-wide scan
+      const bool out_writer = writer && rank == 0;
+      unsigned long long carry = 0ull;
+      for (int base = 0; base < n; base += Tr::kThreads) {
+        const int j = base + tid;
+        unsigned long long P = 0ull;
+        if (j < n) {
+          float acc = 0.f;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float part = 0.f;
-#pragma unroll
-          for (int e = 0; e < E; ++e) part = fmaf(qv[g][e], rv[e], part);
-          part = warp_sum(part);
-          if (lane == 0) es[g * tpc + j0 + j] = ok ? part * p.scale : kNegInf;
+          for (int g = 0; g < G; ++g) {
+            const float sc = es[g * cap + j];
+            acc += sc == kNegInf ? 0.f : expf(sc - s_gm[g]) * s_gz[g];
+          }
+          const float pj = acc / static_cast<float>(G);
+          ps[j] = pj;
+          flag[j] = 0;
+          if (p.team_probs && out_writer) p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = pj;
+          if (pj > 0.f) {
+            const float x = pj * 0x1p62f;                            // exact scaling
+            const unsigned long long fl = __float2ull_rd(x);
+            const float frac = x - __ull2float_rn(fl);               // exact
+            P = fl + (frac >= 0.5f ? 1ull : 0ull);
+          }
         }
+        unsigned long long tot;
+        const unsigned long long v = block_inclusive_scan<unsigned long long>(P, s_wd, tot);
+        if (j < n) cdf[j] = carry + v;
+        carry += tot;
       }
-      __syncthreads();                                  // rows reusable, scores visible
-    }
-    // local per-head (max, sum of exp) over this CTA's teams
-    if (warp < G) {
-      float m = kNegInf;
-      for (int j = lane; j < nl; j += 32) m = fmaxf(m, es[warp * tpc + j]);
-      m = warp_max(m);
-      float z = 0.f;
-      if (m != kNegInf)
-        for (int j = lane; j < nl; j += 32) {
-          const float sc = es[warp * tpc + j];
-          z += sc == kNegInf ? 0.f : expf(sc - m);
-        }
-      z = warp_sum(z);
-      if (lane == 0) {
-        pub.m[warp] = m;
-        pub.z[warp] = z;
-      }
-    }
-    cluster.sync();                                                  // barrier A1
-    if (tid < CL * G) {
-      const Published* peer = cluster.map_shared_rank(&pub, tid / G);
-      s_pm[tid] = peer->m[tid % G];
-      s_pz[tid] = peer->z[tid % G];
-    }
-    __syncthreads();
-    if (tid < G) {
-      float m = kNegInf;
-      for (int r = 0; r < CL; ++r) m = fmaxf(m, s_pm[r * G + tid]);
-      float z = 0.f;
-      if (m != kNegInf)
-        for (int r = 0; r < CL; ++r) {
-          const float mr = s_pm[r * G + tid];
-          z += mr == kNegInf ? 0.f : s_pz[r * G + tid] * expf(mr - m);
-        }
-      s_gm[tid] = m;
-      s_gz[tid] = z;
-    }
-    __syncthreads();
-    // team probabilities p_j = (1/G) sum_g exp(s_gj - m_g) / z_g, and their 62-bit
-    // fixed-point values round(p * 2^62) (ties away from zero)
-    unsigned long long carry = 0;
-    for (int base = 0; base < nl; base += Tr::kThreads) {
-      const int j = base + tid;
-      unsigned long long P = 0;
-      if (j < nl) {
-        float acc = 0.f;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float sc = es[g * tpc + j];
-          acc += (sc == kNegInf || !(s_gz[g] > 0.f)) ? 0.f : expf(sc - s_gm[g]) / s_gz[g];
-        }
-        const float pj = acc / static_cast<float>(G);
-        ps[j] = pj;
-        if (p.team_probs && writer)
-          p.team_probs[static_cast<int64_t>(unit) * p.max_teams + lo + j] = pj;
-        if (pj > 0.f) {
-          const float x = pj * 0x1p62f;                              // exact scaling
-          const unsigned long long fl = __float2ull_rd(x);
-          const float frac = x - __ull2float_rn(fl);                 // exact (x < 2^63)
-          P = fl + (frac >= 0.5f ? 1ull : 0ull);
-        }
-      }
-      unsigned long long tot;
-      const unsigned long long v = block_inclusive_scan<unsigned long long>(P, s_wd, tot);
-      if (j < nl) cdf[j] = carry + v;
-      carry += tot;
-    }
-    if (p.team_probs && writer && rank == 0)
-      for (int j = n + tid; j < p.max_teams; j += Tr::kThreads)
-        p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = 0.f;
-    if (tid == 0) pub.total = nl > 0 ? cdf[nl - 1] : 0ull;
-    cluster.sync();                                                  // barrier A2
-    if (warp == 0) {                                                  // exclusive prefix over ranks
-      const unsigned long long t = lane < CL ? cluster.map_shared_rank(&pub, lane)->total : 0ull;
-      unsigned long long incl = t;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      if (lane == rank) s_off = incl - t;
-      if (lane == 31) s_Z = incl;
-    }
-    __syncthreads();
-    // M draws; the CTA whose slice [off, off + total) holds floor(u Z) resolves the draw
-    const unsigned long long off = s_off, Z = s_Z;
-    const bool valid = len_ok && Z > 0ull;
-    if (valid && nl > 0) {
-      const unsigned long long tot = cdf[nl - 1];
-      const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
-                                   static_cast<uint32_t>(p.seed >> 32));
-      for (int r = tid; r < M; r += Tr::kThreads) {
-        const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(r), static_cast<uint32_t>(h),
-                                                 static_cast<uint32_t>(b), 0u),
-                                      key);
-        const unsigned long long a = 2ull * w.x + 1ull;              // u = a / 2^33
-        const unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
-        if (t >= off && t - off < tot) {
-          const unsigned long long tl = t - off;
-          int lo_i = 0, hi_i = nl - 1;
+      if (p.team_probs && out_writer)
+        for (int j = n + tid; j < p.max_teams; j += Tr::kThreads)
+          p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = 0.f;
+      __syncthreads();
+      // M draws: smallest j with floor(u Z) < C_j
+      const unsigned long long Z = carry;
+      const bool valid = len_ok && Z > 0ull;
+      if (valid) {
+        const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
+                                     static_cast<uint32_t>(p.seed >> 32));
+        for (int r = tid; r < M; r += Tr::kThreads) {
+          const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(r), static_cast<uint32_t>(h),
+                                                   static_cast<uint32_t>(b), 0u),
+                                        key);
+          const unsigned long long a = 2ull * w.x + 1ull;            // u = a / 2^33
+          const unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
+          int lo_i = 0, hi_i = n - 1;
           while (lo_i < hi_i) {
             const int mid = (lo_i + hi_i) >> 1;
-            if (tl < cdf[mid]) hi_i = mid; else lo_i = mid + 1;
+            if (t < cdf[mid]) hi_i = mid; else lo_i = mid + 1;
           }
-          if (writer) p.draw_ids[static_cast<int64_t>(unit) * M + r] = lo + lo_i;
+          if (out_writer) p.draw_ids[static_cast<int64_t>(unit) * M + r] = lo_i;
           flag[lo_i] = 1;
         }
+      } else if (out_writer) {
+        for (int r = tid; r < M; r += Tr::kThreads) p.draw_ids[static_cast<int64_t>(unit) * M + r] = -1;
       }
-    }
-    if (!valid && writer && rank == 0)
-      for (int r = tid; r < M; r += Tr::kThreads) p.draw_ids[static_cast<int64_t>(unit) * M + r] = -1;
-    __syncthreads();
-    // number this CTA's drawn teams and publish them (team, -log2 pi)
-    int count = 0;
-    const float Mf = static_cast<float>(M);
-    for (int base = 0; base < nl; base += Tr::kThreads) {
-      const int j = base + tid;
-      const int f = j < nl ? (flag[j] == 1) : 0;
-      int tot;
-      const int incl = block_inclusive_scan<int>(f, s_wi, tot);
-      if (f) {
-        const int k = count + incl - 1;
-        const float piv = -expm1f(Mf * log1pf(-ps[j]));
-        list[k] = ListEntry{lo + j, -log2f(piv)};
-        flag[j] = k;                       // keep the local slot for the global outputs
-        ps[j] = piv;
-      } else if (j < nl) {
-        flag[j] = -1;
+      __syncthreads();
+      // the distinct drawn teams in ascending order, with pi and -log2 pi
+      const float Mf = static_cast<float>(M);
+      int count = 0;
+      for (int base = 0; base < n; base += Tr::kThreads) {
+        const int j = base + tid;
+        const int f = (valid && j < n) ? (flag[j] == 1) : 0;
+        int tot;
+        const int incl = block_inclusive_scan<int>(f, s_wi, tot);
+        if (f) {
+          const int k = count + incl - 1;
+          const float piv = -expm1f(Mf * log1pf(-ps[j]));
+          llist[k] = ListEntry{j, -log2f(piv)};
+          if (out_writer) {
+            p.sel_ids[static_cast<int64_t>(unit) * M + k] = j;
+            p.pi[static_cast<int64_t>(unit) * M + k] = piv;
+          }
+        }
+        count += tot;
       }
-      count += tot;
-    }
-    if (tid == 0) pub.count = valid ? count : 0;
-    cluster.sync();                                                  // barrier A3
-    if (warp == 0) {
-      const int c = lane < CL ? cluster.map_shared_rank(&pub, lane)->count : 0;
-      int incl = c;
+      if (out_writer) {
+        for (int sidx = count + tid; sidx < M; sidx += Tr::kThreads) {
+          p.sel_ids[static_cast<int64_t>(unit) * M + sidx] = -1;
+          p.pi[static_cast<int64_t>(unit) * M + sidx] = 0.f;
+        }
+        if (tid == 0) p.sel_count[unit] = count;
+      }
+      if (tid == 0) s_base[1] = count;
+      __syncthreads();
+      total_sel = s_base[1];
+    } else {
+      score_teams<D, G>(p, b, h, lo, nl, qs, rows, rows_cap, es, cap, flag);
+      // per-head (max, sum of exp) over the scored teams
+      if (warp < G) {
+        float m = kNegInf;
+        for (int j = lane; j < nl; j += 32) m = fmaxf(m, es[warp * cap + j]);
+        m = warp_max(m);
+        float z = 0.f;
+        if (m != kNegInf)
+          for (int j = lane; j < nl; j += 32) {
+            const float sc = es[warp * cap + j];
+            z += sc == kNegInf ? 0.f : expf(sc - m);
+          }
+        z = warp_sum(z);
+        if (lane == 0) {
+          pub.m[warp] = m;
+          pub.z[warp] = z;
+        }
+      }
+      {
+        cluster.sync();                                                // barrier A1
+        if (tid < CL * G) {
+          const Published* peer = cluster.map_shared_rank(&pub, tid / G);
+          s_pm[tid] = peer->m[tid % G];
+          s_pz[tid] = peer->z[tid % G];
+        }
+        __syncthreads();
+        if (tid < G) {
+          float m = kNegInf;
+          for (int r = 0; r < CL; ++r) m = fmaxf(m, s_pm[r * G + tid]);
+          float z = 0.f;
+          if (m != kNegInf)
+            for (int r = 0; r < CL; ++r) {
+              const float mr = s_pm[r * G + tid];
+              z += mr == kNegInf ? 0.f : s_pz[r * G + tid] * expf(mr - m);
+            }
+          s_gm[tid] = m;
+          s_gz[tid] = z;
+        }
+      }
+      __syncthreads();
+      // team probabilities p_j = (1/G) sum_g exp(s_gj - m_g) / z_g, and their 62-bit
+      // fixed-point values round(p * 2^62) (ties away from zero); inclusive CDF
+      const bool out_writer = writer;
+      unsigned long long carry = 0;
+      for (int base = 0; base < nl; base += Tr::kThreads) {
+        const int j = base + tid;
+        unsigned long long P = 0;
+        if (j < nl) {
+          float acc = 0.f;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-      }
-      if (lane < CL) s_base[lane] = incl - c;
-      if (lane == 31) s_base[CL] = incl;
-    }
-    __syncthreads();
-    total_sel = s_base[CL];
-    if (writer) {
-      if (valid)
-        for (int j = tid; j < nl; j += Tr::kThreads) {
-          if (flag[j] < 0) continue;
-          const int64_t slot = static_cast<int64_t>(unit) * M + s_base[rank] + flag[j];
-          p.sel_ids[slot] = lo + j;
-          p.pi[slot] = ps[j];
+          for (int g = 0; g < G; ++g) {
+            const float sc = es[g * cap + j];
+            acc += (sc == kNegInf || !(s_gz[g] > 0.f)) ? 0.f : expf(sc - s_gm[g]) / s_gz[g];
+          }
+          const float pj = acc / static_cast<float>(G);
+          ps[j] = pj;
+          if (p.team_probs && out_writer)
+            p.team_probs[static_cast<int64_t>(unit) * p.max_teams + lo + j] = pj;
+          if (pj > 0.f) {
+            const float x = pj * 0x1p62f;                              // exact scaling
+            const unsigned long long fl = __float2ull_rd(x);
+            const float frac = x - __ull2float_rn(fl);                 // exact
+            P = fl + (frac >= 0.5f ? 1ull : 0ull);
+          }
         }
-      if (rank == 0) {
-        for (int s = total_sel + tid; s < M; s += Tr::kThreads) {
-          p.sel_ids[static_cast<int64_t>(unit) * M + s] = -1;
-          p.pi[static_cast<int64_t>(unit) * M + s] = 0.f;
-        }
-        if (tid == 0) p.sel_count[unit] = total_sel;
+        unsigned long long tot;
+        const unsigned long long v = block_inclusive_scan<unsigned long long>(P, s_wd, tot);
+        if (j < nl) cdf[j] = carry + v;
+        carry += tot;
       }
+      if (p.team_probs && writer && rank == 0)
+        for (int j = n + tid; j < p.max_teams; j += Tr::kThreads)
+          p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = 0.f;
+      {
+        if (tid == 0) pub.total = nl > 0 ? cdf[nl - 1] : 0ull;
+        cluster.sync();                                                // barrier A2
+        if (warp == 0) {                                                // exclusive prefix over ranks
+          const unsigned long long t = lane < CL ? cluster.map_shared_rank(&pub, lane)->total : 0ull;
+          unsigned long long incl = t;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+          }
+          if (lane == rank) s_off = incl - t;
+          if (lane == 31) s_Z = incl;
+        }
+      }
+      __syncthreads();
+      // M draws; the CTA whose slice [off, off + total) holds floor(u Z) resolves the draw
+      const unsigned long long off = s_off, Z = s_Z;
+      const bool valid = len_ok && Z > 0ull;
+      if (valid && nl > 0) {
+        const unsigned long long tot = cdf[nl - 1];
+        const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
+                                     static_cast<uint32_t>(p.seed >> 32));
+        for (int r = tid; r < M; r += Tr::kThreads) {
+          const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(r), static_cast<uint32_t>(h),
+                                                   static_cast<uint32_t>(b), 0u),
+                                        key);
+          const unsigned long long a = 2ull * w.x + 1ull;              // u = a / 2^33
+          const unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
+          if (t >= off && t - off < tot) {
+            const unsigned long long tl = t - off;
+            int lo_i = 0, hi_i = nl - 1;
+            while (lo_i < hi_i) {
+              const int mid = (lo_i + hi_i) >> 1;
+              if (tl < cdf[mid]) hi_i = mid; else lo_i = mid + 1;
+            }
+            if (out_writer) p.draw_ids[static_cast<int64_t>(unit) * M + r] = lo + lo_i;
+            flag[lo_i] = 1;
+          }
+        }
+      }
+      if (!valid && writer && rank == 0)
+        for (int r = tid; r < M; r += Tr::kThreads) p.draw_ids[static_cast<int64_t>(unit) * M + r] = -1;
+      __syncthreads();
+      // number the drawn teams (ascending) and record them with -log2 pi
+      ListEntry* mylist = list;
+      int count = 0;
+      const float Mf = static_cast<float>(M);
+      for (int base = 0; base < nl; base += Tr::kThreads) {
+        const int j = base + tid;
+        const int f = j < nl ? (flag[j] == 1) : 0;
+        int tot;
+        const int incl = block_inclusive_scan<int>(f, s_wi, tot);
+        if (f) {
+          const int k = count + incl - 1;
+          const float piv = -expm1f(Mf * log1pf(-ps[j]));
+          mylist[k] = ListEntry{lo + j, -log2f(piv)};
+          flag[j] = k;                       // keep the slot for the global outputs
+          ps[j] = piv;
+        } else if (j < nl) {
+          flag[j] = -1;
+        }
+        count += tot;
+      }
+      if (!valid) count = 0;
+      {
+        if (tid == 0) pub.count = count;
+        cluster.sync();                                                // barrier A3
+        if (warp == 0) {
+          const int c = lane < CL ? cluster.map_shared_rank(&pub, lane)->count : 0;
+          int incl = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+          }
+          if (lane < CL) s_base[lane] = incl - c;
+          if (lane == 31) s_base[CL] = incl;
+        }
+      }
+      __syncthreads();
+      total_sel = s_base[CL];
+      if (out_writer) {
+        const int my_base = s_base[rank];
+        if (valid)
+          for (int j = tid; j < nl; j += Tr::kThreads) {
+            if (flag[j] < 0) continue;
+            const int64_t slot = static_cast<int64_t>(unit) * M + my_base + flag[j];
+            p.sel_ids[slot] = lo + j;
+            p.pi[slot] = ps[j];
+          }
+        if (rank == 0) {
+          for (int s = total_sel + tid; s < M; s += Tr::kThreads) {
+            p.sel_ids[static_cast<int64_t>(unit) * M + s] = -1;
+            p.pi[static_cast<int64_t>(unit) * M + s] = 0.f;
+          }
+          if (tid == 0) p.sel_count[unit] = total_sel;
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();                       // sampling scratch is dead from here on
   } else if (mode == kModeAttend) {
     total_sel = p.sel_count[unit];
     if (total_sel < 0 || total_sel > min(M, n)) {
@@ -520,9 +700,14 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
     float lw2 = 0.f;
     bool ok = true;
     if (mode == kModeDecode) {
-      int owner = 0;
-      while (owner + 1 < CL && s_base[owner + 1] <= slot) ++owner;
-      const ListEntry e = cluster.map_shared_rank(list, owner)[slot - s_base[owner]];
+      ListEntry e;
+      if (local) {
+        e = llist[slot];
+      } else {
+        int owner = 0;
+        while (owner + 1 < CL && s_base[owner + 1] <= slot) ++owner;
+        e = cluster.map_shared_rank(list, owner)[slot - s_base[owner]];
+      }
       team = e.team;
       lw2 = e.lw2;
     } else if (mode == kModeAttend) {
@@ -545,180 +730,369 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         ok ? max(0, min(min(p.team_size, L - team * p.team_size) - part * kChunk, kChunk)) : 0;
     table[ci] = ChunkMeta{vt > 0 ? page : -1, vt, lw2, part};
   }
+  fence_proxy_async_smem();      // the ring held phase-A scratch; the copies overwrite it
   __syncthreads();
 
   // ================================================================ phase C: stream + compute
-  // q of the group in registers, in the score layout
-  float qr[G][Tr::kEplS];
-  {
-    const unsigned char* qb = static_cast<const unsigned char*>(p.q) +
-                              (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D * Tr::kEsize;
-#pragma unroll
-    for (int g = 0; g < G; ++g) load_score_row<BF16, D>(qb + g * D * Tr::kEsize, lane16, qr[g]);
-  }
   const unsigned char* kpool = static_cast<const unsigned char*>(p.k_pool);
   const unsigned char* vpool = static_cast<const unsigned char*>(p.v_pool);
   auto issue = [&](int ci) {
     const int stage = ci % S;
     const ChunkMeta m = table[ci];
     if (m.page >= 0) {
-      const int64_t off = ((static_cast<int64_t>(m.page) * p.num_kv_heads + h) *
-                               static_cast<int64_t>(p.team_size) + m.part * kChunk) *
-                          D * Tr::kEsize;
       unsigned char* dst = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
       mbar_arrive_expect_tx(&bar[stage], 2u * Tr::kChunkBytes);
-      bulk_g2s(dst, kpool + off, Tr::kChunkBytes, &bar[stage]);
-      bulk_g2s(dst + Tr::kChunkBytes, vpool + off, Tr::kChunkBytes, &bar[stage]);
+      if constexpr (BF16) {
+        // 64 rows x 64 elements (128 bytes, swizzled) per box; d = 128 takes two boxes
+        const int row = (m.page * p.num_kv_heads + h) * p.team_size + m.part * kChunk;
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx) {
+          tma_load_2d(dst + bx * kChunk * 128, &p.tmap_k, bx * 64, row, &bar[stage]);
+          tma_load_2d(dst + Tr::kChunkBytes + bx * kChunk * 128, &p.tmap_v, bx * 64, row,
+                      &bar[stage]);
+        }
+      } else {
+        const int64_t off = ((static_cast<int64_t>(m.page) * p.num_kv_heads + h) *
+                                 static_cast<int64_t>(p.team_size) + m.part * kChunk) *
+                            D * Tr::kEsize;
+        bulk_g2s(dst, kpool + off, Tr::kChunkBytes, &bar[stage]);
+        bulk_g2s(dst + Tr::kChunkBytes, vpool + off, Tr::kChunkBytes, &bar[stage]);
+      }
     } else {
       mbar_arrive(&bar[stage]);
     }
   };
   if (tid < min(S, n_chunks)) issue(tid);
 
-  const int hh = (lane >> 1) & 7;
-  float m_run = kNegInf, l_run = 0.f;
-  float acc[G][Tr::kEplV];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < Tr::kEplV; ++e) acc[g][e] = 0.f;
-  float* pw = prow + warp * 64;
-  float* aw = arow + warp * kMaxGroup;
-  int consumed = 0;
-
-  for (int ci = 0; ci < n_chunks; ++ci) {
-    const int stage = ci % S;
-    if (!mbar_wait(&bar[stage], (ci / S) & 1)) {
-      set_status(p.status, SANTA_DEV_TIMEOUT);
-      s_abort = 1;
-    }
-    __syncthreads();
-    if (s_abort) break;
-    consumed = ci + 1;
-    const int vt = table[ci].valid;
-    const float lw2 = table[ci].lw2;
-    const unsigned char* ks = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
-    const unsigned char* vs = ks + Tr::kChunkBytes;
-
-    float sc[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int t = warp * 8 + 2 * k + (lane >> 4);
-      float x[Tr::kEplS];
-      load_score_row<BF16, D>(ks + static_cast<size_t>(t) * D * Tr::kEsize, lane16, x);
-      float part[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        part[g] = 0.f;
-        if (g < G) {
-#pragma unroll
-          for (int e = 0; e < Tr::kEplS; ++e) part[g] = fmaf(qr[g][e], x[e], part[g]);
-        }
-      }
-      const float sum = reduce_scatter8(part, lane);
-      sc[k] = (t < vt && hh < G) ? fmaf(sum, p.scale_log2, lw2) : kNegInf;
-    }
-    float cm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
-    const float m_new = fmaxf(m_run, cm);
-    const float alpha = m_new == kNegInf ? 1.f : exp2f(m_run - m_new);
-    float pv[4], psum = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      pv[k] = m_new == kNegInf ? 0.f : exp2f(sc[k] - m_new);
-      psum += pv[k];
-    }
-    psum += __shfl_xor_sync(0xffffffffu, psum, 16);
-    l_run = fmaf(l_run, alpha, psum);
-    m_run = m_new;
-    if (!(lane & 1)) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) pw[(2 * k + (lane >> 4)) * 8 + hh] = pv[k];
-    }
-    if (!(lane & 0x11)) aw[hh] = alpha;
-    __syncwarp();
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float a = aw[g];
-#pragma unroll
-      for (int e = 0; e < Tr::kEplV; ++e) acc[g][e] *= a;
-    }
-    const int nt = min(8, vt - warp * 8);
-#pragma unroll
-    for (int tt = 0; tt < 8; ++tt) {
-      if (tt < nt) {
-        float v[Tr::kEplV];
-        load_value_row<BF16, D>(vs + static_cast<size_t>(warp * 8 + tt) * D * Tr::kEsize, lane,
-                                v);
-        const float4 pa = *reinterpret_cast<const float4*>(pw + tt * 8);
-        const float4 pb = *reinterpret_cast<const float4*>(pw + tt * 8 + 4);
-        const float pg[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int e = 0; e < Tr::kEplV; ++e) acc[g][e] = fmaf(pg[g], v[e], acc[g][e]);
-      }
-    }
-    __syncthreads();
-    if (tid == 0 && ci + S < n_chunks) issue(ci + S);
-  }
-  if (s_abort) {
-    // wait (bounded) for the copies still in flight; contribute nothing
-    if (tid == 0)
-      for (int ci = consumed; ci < min(consumed + S, n_chunks); ++ci)
-        (void)mbar_wait(&bar[ci % S], (ci / S) & 1);
-    m_run = kNegInf;
-    l_run = 0.f;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int e = 0; e < Tr::kEplV; ++e) acc[g][e] = 0.f;
-    __syncthreads();
-  }
-
-  // ================================================================ phase D: combine
   float* mrg_acc = reinterpret_cast<float*>(smem);                   // [8][G][D]
   float* mrg_m = mrg_acc + Tr::kWarps * G * D;                       // [8][8]
   float* mrg_l = mrg_m + Tr::kWarps * kMaxGroup;                     // [8][8]
   float* part = reinterpret_cast<float*>(smem) + Tr::kPartialOff;    // acc [G][D], m [8], l [8]
   float* part_m = part + G * D;
   float* part_l = part_m + kMaxGroup;
-  if (attending) {
+  if constexpr (BF16) {
+    // ---- bf16 K/V: tensor-core scores and P.V (mma.sync m16n8k16, fp32 accumulate)
+    // Warp w owns 16-token tile (w & 3) of every chunk for the scores S^T = K Q^T (the G <= 8
+    // heads are the N = 8 dimension) and half (w >> 2) of d for O^T += V^T P^T.  The chunk's
+    // K and V arrive as 64-row x 128-byte boxes with 128-byte swizzle: 16-byte piece c of row
+    // r sits at piece c ^ (r & 7), so every ldmatrix is conflict-free.  P goes to the second
+    // product as bf16 hi + lo (two MMAs), keeping ~16 bits of it.
+    constexpr int kKS = D / 16;                  // k-steps of the scores
+    constexpr int kDT = D / 32;                  // 16-row d-tiles per half of d
+    constexpr int kBox = kChunk * 128;           // bytes of one 64-row box
+    const int tile = warp & 3, dh = warp >> 2;
+    const int h0 = 2 * (lane & 3);               // this lane's heads h0, h0 + 1
+    const int r0 = 16 * tile + (lane >> 2);      // this lane's tokens r0, r0 + 8
+    uint32_t qfrag[kKS][2];
+    {
+      const int n = lane >> 2, kq = 2 * (lane & 3);
+      const uint16_t* qh = static_cast<const uint16_t*>(p.q) +
+                           (static_cast<int64_t>(b) * p.num_q_heads + h * G + (n < G ? n : 0)) * D;
+#pragma unroll
+      for (int kk = 0; kk < kKS; ++kk) {
+        qfrag[kk][0] = n < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + kq) : 0u;
+        qfrag[kk][1] = n < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + kq) : 0u;
+      }
+    }
+    float o[kDT][4];
+#pragma unroll
+    for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    float mr0 = kNegInf, mr1 = kNegInf, lr0 = 0.f, lr1 = 0.f;
+    int consumed = 0;
+    const int mi = lane >> 3, lr = lane & 7;
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int stage = ci % S;
+      if (!mbar_wait(&bar[stage], (ci / S) & 1)) {
+        set_status(p.status, SANTA_DEV_TIMEOUT);
+        s_abort = 1;
+      }
+      const int vt = table[ci].valid;
+      unsigned char* kst = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
+      __syncthreads();
+      if (s_abort) break;
+      if (vt < kChunk) {                         // rows past the valid tokens: zero V (P = 0)
+        unsigned char* vst = kst + Tr::kChunkBytes;
+        for (int i = tid; i < (kChunk - vt) * 8 * (D / 64); i += Tr::kThreads) {
+          const int bx = i / ((kChunk - vt) * 8), rem = i - bx * (kChunk - vt) * 8;
+          const int row = vt + rem / 8, piece = rem & 7;
+          *reinterpret_cast<uint4*>(vst + bx * kBox + row * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();  // before a later copy into this stage
+        __syncthreads();
+      }
+      consumed = ci + 1;
+      const float lw2 = table[ci].lw2;
+      const uint32_t kb = smem_u32(kst), vb = kb + Tr::kChunkBytes;
+      // scores of tokens r0, r0 + 8 for heads h0, h0 + 1
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < kKS; ++kk) {
+        const int bx = (16 * kk) / 64, c0 = ((16 * kk) & 63) / 8;
+        const int r = 16 * tile + lr + ((mi & 1) << 3), pc = c0 + (mi >> 1);
+        uint32_t a[4];
+        ldmatrix_x4(a, kb + bx * kBox + r * 128 + ((pc ^ (r & 7)) << 4));
+        mma_bf16_16816(c, a, qfrag[kk][0], qfrag[kk][1]);
+      }
+      const bool t0ok = r0 < vt, t1ok = r0 + 8 < vt, g0ok = h0 < G, g1ok = h0 + 1 < G;
+      const float s0 = (t0ok && g0ok) ? fmaf(c[0], p.scale_log2, lw2) : kNegInf;
+      const float s1 = (t0ok && g1ok) ? fmaf(c[1], p.scale_log2, lw2) : kNegInf;
+      const float s2 = (t1ok && g0ok) ? fmaf(c[2], p.scale_log2, lw2) : kNegInf;
+      const float s3 = (t1ok && g1ok) ? fmaf(c[3], p.scale_log2, lw2) : kNegInf;
+      // online softmax per head over the tile's 16 tokens (lanes sharing lane & 3)
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
+      const float al0 = mn0 == kNegInf ? 1.f : exp2f(mr0 - mn0);
+      const float al1 = mn1 == kNegInf ? 1.f : exp2f(mr1 - mn1);
+      const float p0 = mn0 == kNegInf ? 0.f : exp2f(s0 - mn0);
+      const float p1 = mn1 == kNegInf ? 0.f : exp2f(s1 - mn1);
+      const float p2 = mn0 == kNegInf ? 0.f : exp2f(s2 - mn0);
+      const float p3 = mn1 == kNegInf ? 0.f : exp2f(s3 - mn1);
+      float ps0 = p0 + p2, ps1 = p1 + p3;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+      }
+      lr0 = fmaf(lr0, al0, ps0);
+      lr1 = fmaf(lr1, al1, ps1);
+      mr0 = mn0;
+      mr1 = mn1;
+#pragma unroll
+      for (int t = 0; t < kDT; ++t) {
+        o[t][0] *= al0;
+        o[t][1] *= al1;
+        o[t][2] *= al0;
+        o[t][3] *= al1;
+      }
+      // P^T as B fragments: bf16 hi + lo, transposed 8x8 blocks
+      const uint32_t hi01 = pack_bf16(p0, p1), hi23 = pack_bf16(p2, p3);
+      const uint32_t lo01 = pack_bf16(p0 - bf16_lo_f(hi01), p1 - bf16_hi_f(hi01));
+      const uint32_t lo23 = pack_bf16(p2 - bf16_lo_f(hi23), p3 - bf16_hi_f(hi23));
+      const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
+      const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+#pragma unroll
+      for (int t = 0; t < kDT; ++t) {
+        const int d0 = dh * (D / 2) + 16 * t;
+        const int bx = d0 / 64, cd = (d0 & 63) / 8;
+        const int r = 16 * tile + lr + ((mi >> 1) << 3), pc = cd + (mi & 1);
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, vb + bx * kBox + r * 128 + ((pc ^ (r & 7)) << 4));
+        mma_bf16_16816(o[t], a, bh0, bh1);
+        mma_bf16_16816(o[t], a, bl0, bl1);
+      }
+      __syncthreads();
+      if (tid == 0 && ci + S < n_chunks) issue(ci + S);
+    }
+    if (s_abort) {
+      // wait (bounded) for the copies still in flight; contribute nothing
+      if (tid == 0)
+        for (int ci = consumed; ci < min(consumed + S, n_chunks); ++ci)
+          (void)mbar_wait(&bar[ci % S], (ci / S) & 1);
+      mr0 = mr1 = kNegInf;
+      lr0 = lr1 = 0.f;
+#pragma unroll
+      for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+      __syncthreads();
+    }
+    if (attending) {
+      // warp partials: O^T elements (d = d0 + lane/4 (+8), head h0 / h0 + 1), (m, l) per head
+#pragma unroll
+      for (int t = 0; t < kDT; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int d = dh * (D / 2) + 16 * t + (lane >> 2) + ((j >> 1) << 3);
+          const int g = h0 + (j & 1);
+          if (g < G) mrg_acc[(warp * G + g) * D + d] = o[t][j];
+        }
+      if (lane < 4) {
+        mrg_m[warp * kMaxGroup + h0] = mr0;
+        mrg_m[warp * kMaxGroup + h0 + 1] = mr1;
+        mrg_l[warp * kMaxGroup + h0] = lr0;
+        mrg_l[warp * kMaxGroup + h0 + 1] = lr1;
+      }
+      __syncthreads();
+      // CTA partial: the four token tiles of each half of d (both halves share m and l)
+      if (tid < G) {
+        float mx = kNegInf;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mrg_m[w * kMaxGroup + tid]);
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float mw = mrg_m[w * kMaxGroup + tid];
+          l = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_l[w * kMaxGroup + tid], l);
+        }
+        part_m[tid] = mx;
+        part_l[tid] = l;
+      }
+      for (int i = tid; i < G * D; i += Tr::kThreads) {
+        const int g = i / D, k = i - g * D;
+        const int w0 = (k / (D / 2)) * 4;
+        float mx = kNegInf;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mrg_m[(w0 + w) * kMaxGroup + g]);
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float mw = mrg_m[(w0 + w) * kMaxGroup + g];
+          a = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_acc[((w0 + w) * G + g) * D + k], a);
+        }
+        part[i] = a;
+      }
+    }
+  } else {
+    // ---- fp32 K/V: CUDA-core scores and P.V
+    // q of the group in registers, in the score layout
+    float qr[G][Tr::kEplS];
+    {
+      const unsigned char* qbp = static_cast<const unsigned char*>(p.q) +
+                                 (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D * Tr::kEsize;
+#pragma unroll
+      for (int g = 0; g < G; ++g) load_score_row<BF16, D>(qbp + g * D * Tr::kEsize, lane16, qr[g]);
+    }
+    const int hh = (lane >> 1) & 7;
+    float m_run = kNegInf, l_run = 0.f;
+    float acc[G][Tr::kEplV];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int e = 0; e < Tr::kEplV; ++e)
-        mrg_acc[(warp * G + g) * D + lane * Tr::kEplV + e] = acc[g][e];
-    if (!(lane & 0x11)) {
-      mrg_m[warp * kMaxGroup + hh] = m_run;
-      mrg_l[warp * kMaxGroup + hh] = l_run;
-    }
-    __syncthreads();
-    if (tid < G) {
-      float mx = kNegInf;
-#pragma unroll
-      for (int w = 0; w < Tr::kWarps; ++w) mx = fmaxf(mx, mrg_m[w * kMaxGroup + tid]);
-      float l = 0.f;
-#pragma unroll
-      for (int w = 0; w < Tr::kWarps; ++w) {
-        const float mw = mrg_m[w * kMaxGroup + tid];
-        l = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_l[w * kMaxGroup + tid], l);
+      for (int e = 0; e < Tr::kEplV; ++e) acc[g][e] = 0.f;
+    float* pw = prow + warp * 64;
+    float* aw = arow + warp * kMaxGroup;
+    int consumed = 0;
+
+    for (int ci = 0; ci < n_chunks; ++ci) {
+      const int stage = ci % S;
+      if (!mbar_wait(&bar[stage], (ci / S) & 1)) {
+        set_status(p.status, SANTA_DEV_TIMEOUT);
+        s_abort = 1;
       }
-      part_m[tid] = mx;
-      part_l[tid] = l;
-    }
-    for (int i = tid; i < G * D; i += Tr::kThreads) {
-      const int g = i / D, k = i - g * D;
-      float mx = kNegInf;
+      __syncthreads();
+      if (s_abort) break;
+      consumed = ci + 1;
+      const int vt = table[ci].valid;
+      const float lw2 = table[ci].lw2;
+      const unsigned char* ks = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
+      const unsigned char* vs = ks + Tr::kChunkBytes;
+
+      float sc[4];
 #pragma unroll
-      for (int w = 0; w < Tr::kWarps; ++w) mx = fmaxf(mx, mrg_m[w * kMaxGroup + g]);
-      float a = 0.f;
+      for (int k = 0; k < 4; ++k) {
+        const int t = warp * 8 + 2 * k + (lane >> 4);
+        float x[Tr::kEplS];
+        load_score_row<BF16, D>(ks + static_cast<size_t>(t) * D * Tr::kEsize, lane16, x);
+        float part[8];
 #pragma unroll
-      for (int w = 0; w < Tr::kWarps; ++w) {
-        const float mw = mrg_m[w * kMaxGroup + g];
-        a = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_acc[(w * G + g) * D + k], a);
+        for (int g = 0; g < 8; ++g) {
+          part[g] = 0.f;
+          if (g < G) {
+#pragma unroll
+            for (int e = 0; e < Tr::kEplS; ++e) part[g] = fmaf(qr[g][e], x[e], part[g]);
+          }
+        }
+        const float sum = reduce_scatter8(part, lane);
+        sc[k] = (t < vt && hh < G) ? fmaf(sum, p.scale_log2, lw2) : kNegInf;
       }
-      part[i] = a;
+      float cm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+      const float m_new = fmaxf(m_run, cm);
+      const float alpha = m_new == kNegInf ? 1.f : exp2f(m_run - m_new);
+      float pv[4], psum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pv[k] = m_new == kNegInf ? 0.f : exp2f(sc[k] - m_new);
+        psum += pv[k];
+      }
+      psum += __shfl_xor_sync(0xffffffffu, psum, 16);
+      l_run = fmaf(l_run, alpha, psum);
+      m_run = m_new;
+      if (!(lane & 1)) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pw[(2 * k + (lane >> 4)) * 8 + hh] = pv[k];
+      }
+      if (!(lane & 0x11)) aw[hh] = alpha;
+      __syncwarp();
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float a = aw[g];
+#pragma unroll
+        for (int e = 0; e < Tr::kEplV; ++e) acc[g][e] *= a;
+      }
+      const int nt = min(8, vt - warp * 8);
+#pragma unroll
+      for (int tt = 0; tt < 8; ++tt) {
+        if (tt < nt) {
+          float v[Tr::kEplV];
+          load_value_row<BF16, D>(vs + static_cast<size_t>(warp * 8 + tt) * D * Tr::kEsize, lane,
+                                  v);
+          const float4 pa = *reinterpret_cast<const float4*>(pw + tt * 8);
+          const float4 pb = *reinterpret_cast<const float4*>(pw + tt * 8 + 4);
+          const float pg[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < Tr::kEplV; ++e) acc[g][e] = fmaf(pg[g], v[e], acc[g][e]);
+        }
+      }
+      __syncthreads();
+      if (tid == 0 && ci + S < n_chunks) issue(ci + S);
+    }
+    if (s_abort) {
+      // wait (bounded) for the copies still in flight; contribute nothing
+      if (tid == 0)
+        for (int ci = consumed; ci < min(consumed + S, n_chunks); ++ci)
+          (void)mbar_wait(&bar[ci % S], (ci / S) & 1);
+      m_run = kNegInf;
+      l_run = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < Tr::kEplV; ++e) acc[g][e] = 0.f;
+      __syncthreads();
+    }
+
+    if (attending) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < Tr::kEplV; ++e)
+          mrg_acc[(warp * G + g) * D + lane * Tr::kEplV + e] = acc[g][e];
+      if (!(lane & 0x11)) {
+        mrg_m[warp * kMaxGroup + hh] = m_run;
+        mrg_l[warp * kMaxGroup + hh] = l_run;
+      }
+      __syncthreads();
+      if (tid < G) {
+        float mx = kNegInf;
+#pragma unroll
+        for (int w = 0; w < Tr::kWarps; ++w) mx = fmaxf(mx, mrg_m[w * kMaxGroup + tid]);
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < Tr::kWarps; ++w) {
+          const float mw = mrg_m[w * kMaxGroup + tid];
+          l = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_l[w * kMaxGroup + tid], l);
+        }
+        part_m[tid] = mx;
+        part_l[tid] = l;
+      }
+      for (int i = tid; i < G * D; i += Tr::kThreads) {
+        const int g = i / D, k = i - g * D;
+        float mx = kNegInf;
+#pragma unroll
+        for (int w = 0; w < Tr::kWarps; ++w) mx = fmaxf(mx, mrg_m[w * kMaxGroup + g]);
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < Tr::kWarps; ++w) {
+          const float mw = mrg_m[w * kMaxGroup + g];
+          a = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_acc[(w * G + g) * D + k], a);
+        }
+        part[i] = a;
+      }
     }
   }
   cluster.sync();                                                    // barrier D1

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -54,6 +55,10 @@ struct DecodeParams {
   float* part_acc;          // NC > 1: [B*Hkv][NC][G][d]
   uint32_t* counters;       // NC > 1: [B*Hkv], zero between calls
   int32_t* status;
+  // bf16 attending modes: 2-D tensor maps of the K and V pools viewed as
+  // [P*Hkv*T rows][d] with 64-row x 64-element boxes and 128-byte swizzle
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
 };
 
 cudaError_t decode_launch_bf16(const DecodeParams& p, int head_dim, int group, dim3 grid,

@@ -7,6 +7,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "kernels.h"
 
 namespace {
@@ -235,6 +237,37 @@ size_t default_ws_bytes(int dtype, int batch, int hq, int hkv, int d, int T, int
   return ws_bytes_for(units, hq / hkv, d, pl.clusters);
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// A bf16 pool [P][Hkv][T][d] as a 2-D tensor [P*Hkv*T rows][d]: boxes of 64 rows x 64
+// elements (128 bytes, the swizzle span) with 128-byte swizzle.
+int encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int d) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return SANTA_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool),
+                            dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SANTA_OK : SANTA_ERR_CUDA;
+}
+
 int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   int rc = check_inputs(a);
   if (rc) return rc;
@@ -280,6 +313,12 @@ int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   p.part_acc = pl.part_acc;
   p.counters = pl.counters;
   p.status = a->device_status;
+  if (a->dtype == SANTA_BF16 && mode != santa::kModeSample) {
+    const int64_t rows = a->num_pages * a->num_kv_heads * static_cast<int64_t>(a->team_size);
+    if (rows > 0x7fffffffll) return SANTA_ERR_UNSUPPORTED;     // 32-bit row coordinates
+    if ((rc = encode_pool_map(&p.tmap_k, a->k_pool, rows, a->head_dim))) return rc;
+    if ((rc = encode_pool_map(&p.tmap_v, a->v_pool, rows, a->head_dim))) return rc;
+  }
   const dim3 grid(pl.cluster * pl.clusters, a->num_kv_heads, a->batch);
   const int G = a->num_q_heads / a->num_kv_heads;
   const cudaError_t e =
