@@ -47,6 +47,16 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 
 // Makes mbarrier initialisation visible to the asynchronous (bulk copy) proxy.
+// Split cluster barrier; every thread of every CTA of the cluster executes each once, in
+// this order, with no other cluster barrier in between.  The arrive is relaxed: it orders no
+// memory operations, so it may only announce that remote reads whose values the thread has
+// already consumed are over (a returned load cannot observe a later store).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy (bulk
 // copy) accesses of the same bytes; a barrier must follow before the copy is issued.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -84,26 +84,27 @@ struct DecodeTraits {
   static constexpr int kEplV = D / 32;
   static constexpr int kRing = kStages * kStageBytes;
   // phase A scratch inside the ring, for `cap` teams: cdf (uint64), es [8][cap], ps, flag,
-  // the drawn-team list (local path), then rows of representatives (fp32 [rows][D])
-  static constexpr size_t sample_scratch(int cap) {   // rounded up to 128 bytes (the rows
-    return ((sizeof(unsigned long long) + sizeof(float) * kMaxGroup + sizeof(float) +  // take
-             sizeof(int) + sizeof(ListEntry)) * static_cast<size_t>(cap) + 127) /  // 16-byte
-           128 * 128;                                                        // copies)
+  // page ids and the drawn-team list (local path), then rows of representatives (fp32
+  // [rows][D]); rounded up to 128 bytes (the rows take 16-byte copies)
+  static constexpr size_t sample_scratch(int cap) {
+    return ((sizeof(unsigned long long) + sizeof(float) * kMaxGroup + sizeof(float) +
+             2 * sizeof(int) + sizeof(ListEntry)) * static_cast<size_t>(cap) + 127) / 128 * 128;
   }
   static constexpr int rep_rows(int cap) {
     return static_cast<int>((static_cast<size_t>(kRing) - sample_scratch(cap)) / (D * 4));
   }
-  static_assert(rep_rows(kMaxTeamsPerCta) >= 32, "representative buffer must hold 32 rows");
+  static_assert(rep_rows(kMaxTeamsPerCta) >= 16, "representative buffer must hold 16 rows");
   static_assert(sizeof(ListEntry) * kMaxTeamsPerCta >= sizeof(float) * kPubScores,
                 "the list region must hold the published scores");
   // phase D: warp merge buffer [8][G][D] + m, l [8][8], then the CTA partial [G][D] + m, l
   static constexpr int kMergeFloats = kWarps * G * D + 2 * kWarps * kMaxGroup;
   static constexpr int kPartialOff = kMergeFloats;                    // in floats
   static constexpr int kPartialFloats = G * D + 2 * kMaxGroup;
-  static constexpr int kCombOff = kPartialOff + kPartialFloats;         // in floats, 16B aligned
-  static constexpr int kCombFloats = 4 * kThreads;                      // [CL][qb] float4
-  static_assert((kMergeFloats + kPartialFloats + kCombFloats) * 4 <= kRing,
-                "merge buffers must fit");
+  static_assert((kMergeFloats + kPartialFloats) * 4 <= kRing, "merge buffers must fit");
+  // combine buffers in the list region: [CL][ceil(G*D/4/CL)] float4 + [CL][G][2] floats
+  static_assert((G * D / 4 + kMaxCluster) * 16 + kMaxCluster * kMaxGroup * 8 <=
+                    sizeof(ListEntry) * kMaxTeamsPerCta,
+                "combine buffers must fit the list region");
   // dynamic shared memory: ring | list | chunk table | p rows | alpha | bars
   static constexpr size_t kListOff = static_cast<size_t>(kRing);
   static constexpr size_t kTableOff = kListOff + sizeof(ListEntry) * kMaxTeamsPerCta;
@@ -218,31 +219,34 @@ __device__ __forceinline__ V block_inclusive_scan(V v, V* warp_tot, V& block_tot
 }
 
 // Scores s_{g,j} = q_g . rep_j / sqrt(d) of teams [t0, t0 + cnt) of unit (b, h), written
-// to es[g * stride + j] (j relative to t0); flag[j] = -2 marks a team whose page id is out
-// of range (score -inf, status bit), else 0.  The fp32 representative rows are staged in
-// shared memory with 16-byte asynchronous copies issued by every thread (one round trip per
-// batch of `rows_cap` rows); 16 lanes score one team (d/16 elements each, q in registers in
+// to es[g * stride + j] (j relative to t0); pg[j] receives the team's page id, or -2 for a
+// page id out of range (score -inf, status bit).  The page ids of a batch are read in one
+// parallel pass first, so that the 16-byte asynchronous copies of the fp32 representative
+// rows (issued by every thread, one round trip per batch of `rows_cap` rows) do not each
+// wait on a dependent load; 16 lanes score one team (d/16 elements each, q in registers in
 // the same layout) and an 8-shuffle reduce-scatter leaves lane l with head (l >> 1) & 7.
 template <int D, int G>
 __device__ __forceinline__ void score_teams(const DecodeParams& p, int b, int h, int t0, int cnt,
                                             const float (&qs)[G][D / 16], float* rows,
-                                            int rows_cap, float* es, int stride, int* flag) {
+                                            int rows_cap, float* es, int stride, int* pg) {
   constexpr int kQuads = D / 4;                    // 16-byte pieces of a row
   constexpr float kNegInf = -INFINITY;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, lane16 = lane & 15;
   const int hh = (lane >> 1) & 7;
   for (int j0 = 0; j0 < cnt; j0 += rows_cap) {
     const int bc = min(rows_cap, cnt - j0);
+    for (int j = tid; j < bc; j += 256) {
+      const int page = p.page_table[static_cast<int64_t>(b) * p.max_teams + t0 + j0 + j];
+      const bool ok = page >= 0 && page < p.num_pages;
+      if (!ok) set_status(p.status, SANTA_DEV_BAD_PAGE);
+      pg[j0 + j] = ok ? page : -2;
+    }
+    __syncthreads();
     for (int c = tid; c < bc * kQuads; c += 256) {
       const int j = c / kQuads, k = c - j * kQuads;
-      const int64_t page = p.page_table[static_cast<int64_t>(b) * p.max_teams + t0 + j0 + j];
-      const bool ok = page >= 0 && page < p.num_pages;
-      if (k == 0) {
-        flag[j0 + j] = ok ? 0 : -2;
-        if (!ok) set_status(p.status, SANTA_DEV_BAD_PAGE);
-      }
+      const int64_t page = max(pg[j0 + j], 0);
       cp_async16(rows + static_cast<size_t>(j) * D + 4 * k,
-                 p.reps + ((ok ? page : 0) * p.num_kv_heads + h) * D + 4 * k);
+                 p.reps + (page * p.num_kv_heads + h) * D + 4 * k);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -267,7 +271,7 @@ __device__ __forceinline__ void score_teams(const DecodeParams& p, int b, int h,
       }
       const float sum = reduce_scatter8(part, lane);
       if (j < bc && !(lane & 1) && hh < G)
-        es[hh * stride + j0 + j] = flag[j0 + j] == 0 ? sum * p.scale : kNegInf;
+        es[hh * stride + j0 + j] = pg[j0 + j] >= 0 ? sum * p.scale : kNegInf;
     }
     __syncthreads();                               // rows may be refilled
   }
@@ -341,18 +345,22 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
   // further exchange.  Shapes whose slice scores do not fit the region use the
   // distributed path (softmax statistics, CDF totals and counts exchanged in three rounds).
   const int per = (n + CL - 1) / CL;
-  const bool local = G * per <= kPubScores && n <= kMaxTeamsPerCta;
+  const bool local = (G + 1) * per <= kPubScores && n <= kMaxTeamsPerCta;
   ListEntry* llist = nullptr;             // local sampling: the drawn teams, in slot order
+  const int* lpages = nullptr;            // local sampling: page id of every team of the unit
   if (sampling) {
     const int cap = local ? max(n, 1) : p.teams_per_cta;
     unsigned long long* cdf = reinterpret_cast<unsigned long long*>(smem);   // [cap]
     float* es = reinterpret_cast<float*>(cdf + cap);                 // [8][cap] scores, exps
     float* ps = es + kMaxGroup * cap;                                // [cap] team probability
     int* flag = reinterpret_cast<int*>(ps + cap);                    // [cap] drawn / slot
-    llist = reinterpret_cast<ListEntry*>(flag + cap);                // [cap]
+    int* pages = flag + cap;                                         // [cap] page ids (local)
+    llist = reinterpret_cast<ListEntry*>(pages + cap);               // [cap]
+    if (local) lpages = pages;
     float* rows = reinterpret_cast<float*>(smem + Tr::sample_scratch(cap));
     const int rows_cap = Tr::rep_rows(cap);
     float* pub_scores = reinterpret_cast<float*>(list);              // [G][per], published
+    int* pub_pages = reinterpret_cast<int*>(pub_scores + G * per);   // [per], published
     int lo = min(rank * per, n);
     int nl = min(lo + per, n) - lo;
     // q of the group in registers, in the fp32 score layout
@@ -369,66 +377,108 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         }
     }
     if (local) {
-      score_teams<D, G>(p, b, h, lo, nl, qs, rows, rows_cap, pub_scores, per, flag);
-      cluster.sync();                                                // barrier S1
-      // all peers' published scores [G][per] into es [G][cap]: 16-byte DSMEM reads when the
-      // slice length allows, one parallel round trip
-      if ((per & 3) == 0) {
-        const int q4 = G * per / 4;                                  // float4 per peer
-        for (int i = tid; i < CL * q4; i += Tr::kThreads) {
-          const int r = i / q4, k = (i - r * q4) * 4;
-          const int g = k / per, jj = k - g * per, j = r * per + jj;
-          const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(pub_scores, r) + k);
-          float* dst = es + g * cap + j;
-          if (j + 3 < n) {
-            dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
-          } else {
-            if (j < n) dst[0] = v.x;
-            if (j + 1 < n) dst[1] = v.y;
-            if (j + 2 < n) dst[2] = v.z;
-          }
-        }
-      } else {
-        for (int i = tid; i < G * n; i += Tr::kThreads) {
-          const int g = i / n, j = i - g * n;
-          const int r = j / per;
-          es[g * cap + j] = cluster.map_shared_rank(pub_scores, r)[g * per + (j - r * per)];
-        }
-      }
-      __syncthreads();
-      // per-head max and sum of exp over all n teams: one warp per head
+      score_teams<D, G>(p, b, h, lo, nl, qs, rows, rows_cap, pub_scores, per, pub_pages);
+      // the slice's per-head max and sum of exp, published with the scores
       if (warp < G) {
         float m = kNegInf;
-        for (int j = lane; j < n; j += 32) m = fmaxf(m, es[warp * cap + j]);
+        for (int j = lane; j < nl; j += 32) m = fmaxf(m, pub_scores[warp * per + j]);
         m = warp_max(m);
         float z = 0.f;
         if (m != kNegInf)
-          for (int j = lane; j < n; j += 32) {
-            const float sc = es[warp * cap + j];
+          for (int j = lane; j < nl; j += 32) {
+            const float sc = pub_scores[warp * per + j];
             z += sc == kNegInf ? 0.f : expf(sc - m);
           }
         z = warp_sum(z);
         if (lane == 0) {
+          pub.m[warp] = m;
+          pub.z[warp] = z;
+        }
+      }
+      cluster.sync();                                                // barrier S1
+      // every peer's (m, z), scores [G][per] and page ids [per] into this CTA: all remote
+      // reads of a thread issued before its stores (16-byte words when per allows)
+      float pm = 0.f, pz = 0.f;
+      if (tid < CL * G) {
+        const Published* peer = cluster.map_shared_rank(&pub, tid / G);
+        pm = peer->m[tid % G];
+        pz = peer->z[tid % G];
+      }
+      const int words = (G + 1) * per;                               // per peer
+      if ((per & 3) == 0) {
+        const int q4 = words / 4, tot4 = CL * q4;
+        for (int i0 = tid; i0 < tot4; i0 += 4 * Tr::kThreads) {
+          uint4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * Tr::kThreads;
+            if (i < tot4) {
+              const int r = i / q4, k = (i - r * q4) * 4;
+              v[u] = *reinterpret_cast<const uint4*>(
+                  reinterpret_cast<const uint32_t*>(cluster.map_shared_rank(pub_scores, r)) + k);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * Tr::kThreads;
+            if (i < tot4) {
+              const int r = i / q4, k = (i - r * q4) * 4;
+              const int g = k / per, j = r * per + (k - g * per);
+              uint32_t* dst = g < G ? reinterpret_cast<uint32_t*>(es + g * cap) + j
+                                    : reinterpret_cast<uint32_t*>(pages) + j;
+              if (j < n) dst[0] = v[u].x;
+              if (j + 1 < n) dst[1] = v[u].y;
+              if (j + 2 < n) dst[2] = v[u].z;
+              if (j + 3 < n) dst[3] = v[u].w;
+            }
+          }
+        }
+      } else {
+        for (int i = tid; i < (G + 1) * n; i += Tr::kThreads) {
+          const int g = i / n, j = i - g * n;
+          const int r = j / per;
+          const uint32_t w = reinterpret_cast<const uint32_t*>(
+              cluster.map_shared_rank(pub_scores, r))[g * per + (j - r * per)];
+          if (g < G) reinterpret_cast<uint32_t*>(es)[g * cap + j] = w;
+          else pages[j] = static_cast<int>(w);
+        }
+      }
+      if (tid < CL * G) {
+        s_pm[tid] = pm;
+        s_pz[tid] = pz;
+      }
+      __syncthreads();
+      // per-head max and sum of exp over all n teams from the CL slices: warp g, lane r;
+      // s_gz holds 1 / (G z) so that p_j is a plain weighted sum
+      if (warp < G) {
+        const float mr = lane < CL ? s_pm[lane * G + warp] : kNegInf;
+        const float m = warp_max(mr);
+        const float zr = (lane < CL && mr != kNegInf) ? s_pz[lane * G + warp] * expf(mr - m) : 0.f;
+        const float z = warp_sum(zr);
+        if (lane == 0) {
           s_gm[warp] = m;
-          s_gz[warp] = z > 0.f ? 1.f / z : 0.f;                       // reciprocal
+          s_gz[warp] = z > 0.f ? 1.f / (z * static_cast<float>(G)) : 0.f;
         }
       }
       __syncthreads();
-      // p_j = (1/G) sum_g exp(s_gj - m_g) / z_g, round(p_j 2^62) and the exact integer CDF,
-      // 256 teams per block-wide scan
+      // p_j = (1/G) sum_g exp(s_gj - m_g) / z_g, round(p_j 2^62) and the exact integer CDF:
+      // thread t takes teams [t*tpt, (t+1)*tpt), a serial sum, then one block-wide scan
+      constexpr int kTpt = kMaxTeamsPerCta / Tr::kThreads;
+      const int tpt = (n + Tr::kThreads - 1) / Tr::kThreads;          // <= kTpt
+      const int jt = tid * tpt;
       const bool out_writer = writer && rank == 0;
-      unsigned long long carry = 0ull;
-      for (int base = 0; base < n; base += Tr::kThreads) {
-        const int j = base + tid;
+      unsigned long long run = 0ull, incl_t[kTpt];
+#pragma unroll
+      for (int u = 0; u < kTpt; ++u) {
+        const int j = jt + u;
         unsigned long long P = 0ull;
-        if (j < n) {
-          float acc = 0.f;
+        if (u < tpt && j < n) {
+          float pj = 0.f;
 #pragma unroll
           for (int g = 0; g < G; ++g) {
             const float sc = es[g * cap + j];
-            acc += sc == kNegInf ? 0.f : expf(sc - s_gm[g]) * s_gz[g];
+            pj += sc == kNegInf ? 0.f : expf(sc - s_gm[g]) * s_gz[g];
           }
-          const float pj = acc / static_cast<float>(G);
           ps[j] = pj;
           flag[j] = 0;
           if (p.team_probs && out_writer) p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = pj;
@@ -439,17 +489,19 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
             P = fl + (frac >= 0.5f ? 1ull : 0ull);
           }
         }
-        unsigned long long tot;
-        const unsigned long long v = block_inclusive_scan<unsigned long long>(P, s_wd, tot);
-        if (j < n) cdf[j] = carry + v;
-        carry += tot;
+        run += P;
+        incl_t[u] = run;
       }
+      unsigned long long Z;
+      const unsigned long long before = block_inclusive_scan<unsigned long long>(run, s_wd, Z) - run;
+#pragma unroll
+      for (int u = 0; u < kTpt; ++u)
+        if (u < tpt && jt + u < n) cdf[jt + u] = before + incl_t[u];
       if (p.team_probs && out_writer)
         for (int j = n + tid; j < p.max_teams; j += Tr::kThreads)
           p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = 0.f;
       __syncthreads();
       // M draws: smallest j with floor(u Z) < C_j
-      const unsigned long long Z = carry;
       const bool valid = len_ok && Z > 0ull;
       if (valid) {
         const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
@@ -472,24 +524,27 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         for (int r = tid; r < M; r += Tr::kThreads) p.draw_ids[static_cast<int64_t>(unit) * M + r] = -1;
       }
       __syncthreads();
-      // the distinct drawn teams in ascending order, with pi and -log2 pi
+      // the distinct drawn teams in ascending order, with pi and -log2 pi (same team split
+      // over threads as the CDF, one block-wide scan)
       const float Mf = static_cast<float>(M);
-      int count = 0;
-      for (int base = 0; base < n; base += Tr::kThreads) {
-        const int j = base + tid;
-        const int f = (valid && j < n) ? (flag[j] == 1) : 0;
-        int tot;
-        const int incl = block_inclusive_scan<int>(f, s_wi, tot);
-        if (f) {
-          const int k = count + incl - 1;
+      int mine = 0;
+#pragma unroll
+      for (int u = 0; u < kTpt; ++u)
+        if (valid && u < tpt && jt + u < n && flag[jt + u] == 1) ++mine;
+      int count;
+      int k = block_inclusive_scan<int>(mine, s_wi, count) - mine;
+#pragma unroll
+      for (int u = 0; u < kTpt; ++u) {
+        const int j = jt + u;
+        if (valid && u < tpt && j < n && flag[j] == 1) {
           const float piv = -expm1f(Mf * log1pf(-ps[j]));
           llist[k] = ListEntry{j, -log2f(piv)};
           if (out_writer) {
             p.sel_ids[static_cast<int64_t>(unit) * M + k] = j;
             p.pi[static_cast<int64_t>(unit) * M + k] = piv;
           }
+          ++k;
         }
-        count += tot;
       }
       if (out_writer) {
         for (int sidx = count + tid; sidx < M; sidx += Tr::kThreads) {
@@ -498,9 +553,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         }
         if (tid == 0) p.sel_count[unit] = count;
       }
-      if (tid == 0) s_base[1] = count;
       __syncthreads();
-      total_sel = s_base[1];
+      total_sel = count;
     } else {
       score_teams<D, G>(p, b, h, lo, nl, qs, rows, rows_cap, es, cap, flag);
       // per-head (max, sum of exp) over the scored teams
@@ -558,6 +612,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
           }
           const float pj = acc / static_cast<float>(G);
           ps[j] = pj;
+          flag[j] = 0;                                                 // held page ids
           if (p.team_probs && out_writer)
             p.team_probs[static_cast<int64_t>(unit) * p.max_teams + lo + j] = pj;
           if (pj > 0.f) {
@@ -720,7 +775,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
     }
     int page = -1;
     if (ok) {
-      page = p.page_table[static_cast<int64_t>(b) * p.max_teams + team];
+      page = lpages ? lpages[team] : p.page_table[static_cast<int64_t>(b) * p.max_teams + team];
       if (page < 0 || page >= p.num_pages) {
         set_status(p.status, SANTA_DEV_BAD_PAGE);
         ok = false;
@@ -732,6 +787,10 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
   }
   fence_proxy_async_smem();      // the ring held phase-A scratch; the copies overwrite it
   __syncthreads();
+  // Split cluster barrier: this CTA has finished every read of its peers' shared memory
+  // (published scores, drawn-team lists).  The matching wait comes after the streaming loop,
+  // before partials are pushed into the peers' list regions.
+  cluster_arrive_relaxed();
 
   // ================================================================ phase C: stream + compute
   const unsigned char* kpool = static_cast<const unsigned char*>(p.k_pool);
@@ -916,7 +975,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         mrg_l[warp * kMaxGroup + h0 + 1] = lr1;
       }
       __syncthreads();
-      // CTA partial: the four token tiles of each half of d (both halves share m and l)
+      // CTA partial: the four token tiles of each half of d (both halves share m and l);
+      // the tile weights exp2(m_t - m) once per head
       if (tid < G) {
         float mx = kNegInf;
 #pragma unroll
@@ -925,23 +985,21 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const float mw = mrg_m[w * kMaxGroup + tid];
-          l = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_l[w * kMaxGroup + tid], l);
+          const float wt = mw == kNegInf ? 0.f : exp2f(mw - mx);
+          arow[w * kMaxGroup + tid] = wt;
+          l = fmaf(wt, mrg_l[w * kMaxGroup + tid], l);
         }
         part_m[tid] = mx;
         part_l[tid] = l;
       }
+      __syncthreads();
       for (int i = tid; i < G * D; i += Tr::kThreads) {
         const int g = i / D, k = i - g * D;
         const int w0 = (k / (D / 2)) * 4;
-        float mx = kNegInf;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mrg_m[(w0 + w) * kMaxGroup + g]);
         float a = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float mw = mrg_m[(w0 + w) * kMaxGroup + g];
-          a = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_acc[((w0 + w) * G + g) * D + k], a);
-        }
+        for (int w = 0; w < 4; ++w)
+          a = fmaf(arow[w * kMaxGroup + g], mrg_acc[((w0 + w) * G + g) * D + k], a);
         part[i] = a;
       }
     }
@@ -1095,80 +1153,73 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
       }
     }
   }
-  cluster.sync();                                                    // barrier D1
+  // ---- combine: each CTA pushes the quads of its partial that rank r owns, with its (m, l),
+  // into rank r's list region (remote stores, no round trip); one cluster barrier; each CTA
+  // then merges its slice of the G*D outputs from local shared memory, in rank order.
+  constexpr int kQuads = G * D / 4;
+  const int qper = (kQuads + CL - 1) / CL;
+  float4* comb_q = reinterpret_cast<float4*>(list);                 // [CL][qper] partial quads
+  float* comb_ml = reinterpret_cast<float*>(comb_q + CL * qper);    // [CL][G][2] (m, l)
+  __syncthreads();                                                  // part complete
+  cluster_wait();                                                   // peers' reads are done
+  if (attending) {
+    for (int qi = tid; qi < kQuads; qi += Tr::kThreads) {
+      const int r = qi / qper, k = qi - r * qper;
+      cluster.map_shared_rank(comb_q, r)[rank * qper + k] = reinterpret_cast<const float4*>(part)[qi];
+    }
+    if (tid < CL * G) {
+      const int r = tid / G, g = tid - r * G;
+      float* dst = cluster.map_shared_rank(comb_ml, r) + (rank * G + g) * 2;
+      dst[0] = part_m[g];
+      dst[1] = part_l[g];
+    }
+    cluster.sync();                                                 // barrier D1: delivered
+  }
   float* out_unit = p.out + (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D;
   if (attending) {
-    // cluster-wide weights: peers' (m, l) per head
-    if (tid < CL * G) {
-      const float* peer = cluster.map_shared_rank(part, tid / G);
-      s_pm[tid] = peer[G * D + tid % G];
-      s_pz[tid] = peer[G * D + kMaxGroup + tid % G];
-    }
-    __syncthreads();
-    if (tid < G) {
-      float mx = kNegInf;
-      for (int r = 0; r < CL; ++r) mx = fmaxf(mx, s_pm[r * G + tid]);
-      float l = 0.f;
-      for (int r = 0; r < CL; ++r) {
-        const float mr = s_pm[r * G + tid];
-        const float w = mr == kNegInf ? 0.f : exp2f(mr - mx);
-        s_pm[r * G + tid] = w;                                       // becomes the weight
-        l = fmaf(w, s_pz[r * G + tid], l);
+    // weights of the CL partials per head: warp g, lane r
+    if (warp < G) {
+      const float mr = lane < CL ? comb_ml[(lane * G + warp) * 2] : kNegInf;
+      const float mx = warp_max(mr);
+      const float w = mr == kNegInf ? 0.f : exp2f(mr - mx);
+      if (lane < CL) s_pm[lane * G + warp] = w;
+      const float l = warp_sum(lane < CL ? w * comb_ml[(lane * G + warp) * 2 + 1] : 0.f);
+      if (lane == 0) {
+        s_gm[warp] = mx;
+        s_gz[warp] = l;
       }
-      s_gm[tid] = mx;
-      s_gz[tid] = l;
     }
     __syncthreads();
-    // this CTA's slice of the G*D/4 output quads: one thread per (peer, quad) fetches that
-    // peer's weighted partial quad (all remote reads in flight at once), then per-quad sums
-    // in rank order
-    constexpr int kQuads = G * D / 4;
-    const int qper = (kQuads + CL - 1) / CL;
     const int q0 = min(rank * qper, kQuads);
     const int nq = min(q0 + qper, kQuads) - q0;
-    const int qb = Tr::kThreads / CL;                                // quads per block
-    float4* comb = reinterpret_cast<float4*>(reinterpret_cast<float*>(smem) + Tr::kCombOff);
-    for (int base = 0; base < nq; base += qb) {
-      const int nb = min(qb, nq - base);
-      {
-        const int r = tid / qb, k = tid - r * qb;
-        if (r < CL && k < nb) {
-          const int qi = q0 + base + k;
-          const float w = s_pm[r * G + (qi * 4) / D];
-          const float4 v = reinterpret_cast<const float4*>(cluster.map_shared_rank(part, r))[qi];
-          comb[r * qb + k] = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
-        }
+    for (int k = tid; k < nq; k += Tr::kThreads) {
+      const int qi = q0 + k;
+      const int g = (qi * 4) / D;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int r = 0; r < CL; ++r) {
+        const float w = s_pm[r * G + g];
+        const float4 v = comb_q[r * qper + k];
+        a.x = fmaf(w, v.x, a.x);
+        a.y = fmaf(w, v.y, a.y);
+        a.z = fmaf(w, v.z, a.z);
+        a.w = fmaf(w, v.w, a.w);
       }
-      __syncthreads();
-      if (tid < nb) {
-        const int qi = q0 + base + tid;
-        const int g = (qi * 4) / D;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r = 0; r < CL; ++r) {
-          const float4 v = comb[r * qb + tid];
-          a.x += v.x;
-          a.y += v.y;
-          a.z += v.z;
-          a.w += v.w;
-        }
-        if (NC == 1) {
-          const float l = s_gz[g];
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          reinterpret_cast<float4*>(out_unit)[qi] =
-              make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
-        } else {
-          reinterpret_cast<float4*>(p.part_acc +
-                                    (static_cast<int64_t>(unit) * NC + cidx) * G * D)[qi] = a;
-        }
+      if (NC == 1) {
+        const float l = s_gz[g];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        reinterpret_cast<float4*>(out_unit)[qi] =
+            make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+      } else {
+        reinterpret_cast<float4*>(p.part_acc +
+                                  (static_cast<int64_t>(unit) * NC + cidx) * G * D)[qi] = a;
       }
-      __syncthreads();
     }
     if (NC > 1 && rank == 0 && tid < G) {
       p.part_ml[((static_cast<int64_t>(unit) * NC + cidx) * G + tid) * 2] = s_gm[tid];
       p.part_ml[((static_cast<int64_t>(unit) * NC + cidx) * G + tid) * 2 + 1] = s_gz[tid];
     }
   }
-  cluster.sync();                                                    // barrier D2: peers done
   if (!attending || NC == 1) return;
 
   // ---- several clusters per unit: the last CTA to arrive merges the cluster partials
@@ -1197,7 +1248,6 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
     s_gz[tid] = l;
   }
   __syncthreads();
-  constexpr int kQuads = G * D / 4;
   for (int qi = tid; qi < kQuads; qi += Tr::kThreads) {
     const int g = (qi * 4) / D;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
