@@ -230,9 +230,10 @@ int santa_dense_decode(const santa_decode_args* a, void* stream);
  *     the scratch holds (santa_decode_workspace_min_bytes > santa_noalloc_scratch_bytes).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *     with that device current; make that first call before any stream capture.
- *   - Every call on a device shares the one array; the arrival counters in it are reset by
- *     the sampling kernel of each call.  Calls whose kernels overlap on the GPU (different
- *     streams, or other threads) race on it: serialise them.
+ *   - Every call on a device shares the one array, which keeps the previous call's
+ *     contents; each call first clears the arrival counters in it (cudaMemsetAsync on the
+ *     call's stream, no allocation).  Calls whose work overlaps on the GPU (different
+ *     streams, or other threads) race on the array: serialise them.
  */
 int santa_decode_noalloc(const santa_decode_args* a, void* stream);
 

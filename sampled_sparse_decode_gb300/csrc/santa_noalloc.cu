@@ -12,14 +12,16 @@
 
 #include "kernels.h"
 
-namespace {
-
 // Upper bound of the scratch this entry point can use.  4 MiB holds the default split plan
 // of every workload in this repository (about 1 MiB each); larger problems run with fewer,
 // longer splits, and problems whose minimum need exceeds it are rejected.
-constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+static constexpr size_t kStaticScratchBytes = size_t(4) << 20;
 
-__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+// The scratch itself: zero-initialised when the module loads on a device.  In host code
+// this name is only a stand-in; kernels get the address from scratch_address().
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
 
 // Device address of g_static_scratch on each device, looked up once per device (the host
 // symbol itself is only a stand-in and must never be handed to a kernel).
@@ -51,6 +53,14 @@ extern "C" int santa_decode_noalloc(const santa_decode_args* a, void* stream) {
   if (need > kStaticScratchBytes) return SANTA_ERR_SCRATCH_LIMIT;
   void* scratch = scratch_address();
   if (!scratch) return SANTA_ERR_CUDA;
+  // The array keeps the previous call's contents.  Partials are always written before they
+  // are read, but the arrival counters at its start (one 32-bit word per unit, padded to
+  // 256 bytes; the array is 256-byte aligned, so the split plan puts them at offset 0) must
+  // start at zero: clear them on the call's stream.
+  const size_t units = static_cast<size_t>(a->batch) * static_cast<size_t>(a->num_kv_heads);
+  const size_t counters = (units * sizeof(uint32_t) + 255) / 256 * 256;
+  if (cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SANTA_ERR_CUDA;
   santa_decode_args b = *a;
   b.workspace = scratch;
   b.workspace_bytes = kStaticScratchBytes;
