@@ -218,6 +218,31 @@ __device__ __forceinline__ V block_inclusive_scan(V v, V* warp_tot, V& block_tot
   return res;
 }
 
+// Exclusive scan of one value per thread over the 256-thread block with a single barrier:
+// every warp sums the 8 warp totals itself (fixed order).  `total` receives the block sum.
+// warp_tot must not be written again before another block-wide barrier.
+template <typename V>
+__device__ __forceinline__ V block_exclusive_scan(V v, V* warp_tot, V& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  V incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const V t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  V pre = V(0), tot = V(0);
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const V t = warp_tot[w];
+    if (w < warp) pre += t;
+    tot += t;
+  }
+  total = tot;
+  return pre + incl - v;
+}
+
 // Scores s_{g,j} = q_g . rep_j / sqrt(d) of teams [t0, t0 + cnt) of unit (b, h), written
 // to es[g * stride + j] (j relative to t0); pg[j] receives the team's page id, or -2 for a
 // page id out of range (score -inf, status bit).  The page ids of a batch are read in one
@@ -349,7 +374,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
   ListEntry* llist = nullptr;             // local sampling: the drawn teams, in slot order
   const int* lpages = nullptr;            // local sampling: page id of every team of the unit
   if (sampling) {
-    const int cap = local ? max(n, 1) : p.teams_per_cta;
+    const int cap = local ? (max(n, 1) + 3) / 4 * 4 : p.teams_per_cta;   // rows 16-byte aligned
     unsigned long long* cdf = reinterpret_cast<unsigned long long*>(smem);   // [cap]
     float* es = reinterpret_cast<float*>(cdf + cap);                 // [8][cap] scores, exps
     float* ps = es + kMaxGroup * cap;                                // [cap] team probability
@@ -377,108 +402,87 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         }
     }
     if (local) {
+      // Split cluster barrier, arrive: this CTA runs.  The wait below, before the first
+      // remote store, guarantees that every peer runs too.
+      cluster_arrive_relaxed();
       score_teams<D, G>(p, b, h, lo, nl, qs, rows, rows_cap, pub_scores, per, pub_pages);
-      // the slice's per-head max and sum of exp, published with the scores
+      // the slice's per-head max m_r and sum of exp z_r; the staged scores become
+      // e = exp(s - m_r), so that p needs no further exponentials once m and z are known
       if (warp < G) {
         float m = kNegInf;
         for (int j = lane; j < nl; j += 32) m = fmaxf(m, pub_scores[warp * per + j]);
         m = warp_max(m);
         float z = 0.f;
-        if (m != kNegInf)
-          for (int j = lane; j < nl; j += 32) {
-            const float sc = pub_scores[warp * per + j];
-            z += sc == kNegInf ? 0.f : expf(sc - m);
-          }
+        for (int j = lane; j < nl; j += 32) {
+          const float sc = pub_scores[warp * per + j];
+          const float e = (m == kNegInf || sc == kNegInf) ? 0.f : expf(sc - m);
+          pub_scores[warp * per + j] = e;
+          z += e;
+        }
         z = warp_sum(z);
         if (lane == 0) {
           pub.m[warp] = m;
           pub.z[warp] = z;
         }
       }
-      cluster.sync();                                                // barrier S1
-      // every peer's (m, z), scores [G][per] and page ids [per] into this CTA: all remote
-      // reads of a thread issued before its stores (16-byte words when per allows)
-      float pm = 0.f, pz = 0.f;
-      if (tid < CL * G) {
-        const Published* peer = cluster.map_shared_rank(&pub, tid / G);
-        pm = peer->m[tid % G];
-        pz = peer->z[tid % G];
-      }
-      const int words = (G + 1) * per;                               // per peer
+      __syncthreads();
+      // push the slice (e rows [G][per], page ids [per]) and (m_r, z_r) into every CTA of the
+      // cluster (this one included): remote stores, no round trip; barrier S1 publishes them
+      cluster_wait();
       if ((per & 3) == 0) {
-        const int q4 = words / 4, tot4 = CL * q4;
-        for (int i0 = tid; i0 < tot4; i0 += 4 * Tr::kThreads) {
-          uint4 v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * Tr::kThreads;
-            if (i < tot4) {
-              const int r = i / q4, k = (i - r * q4) * 4;
-              v[u] = *reinterpret_cast<const uint4*>(
-                  reinterpret_cast<const uint32_t*>(cluster.map_shared_rank(pub_scores, r)) + k);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * Tr::kThreads;
-            if (i < tot4) {
-              const int r = i / q4, k = (i - r * q4) * 4;
-              const int g = k / per, j = r * per + (k - g * per);
-              uint32_t* dst = g < G ? reinterpret_cast<uint32_t*>(es + g * cap) + j
-                                    : reinterpret_cast<uint32_t*>(pages) + j;
-              if (j < n) dst[0] = v[u].x;
-              if (j + 1 < n) dst[1] = v[u].y;
-              if (j + 2 < n) dst[2] = v[u].z;
-              if (j + 3 < n) dst[3] = v[u].w;
-            }
-          }
+        const int q = per / 4;                                       // 16-byte words per row
+        const int items = CL * (G + 1) * q;
+        for (int i = tid; i < items; i += Tr::kThreads) {
+          const int r = i / ((G + 1) * q), k = i - r * (G + 1) * q;
+          const int g = k / q, jj = 4 * (k - g * q);
+          if (jj >= nl) continue;
+          const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(pub_scores) + g * per + jj);
+          uint32_t* dst = g < G ? reinterpret_cast<uint32_t*>(es + g * cap) : reinterpret_cast<uint32_t*>(pages);
+          *reinterpret_cast<uint4*>(cluster.map_shared_rank(dst, r) + lo + jj) = v;
         }
       } else {
-        for (int i = tid; i < (G + 1) * n; i += Tr::kThreads) {
-          const int g = i / n, j = i - g * n;
-          const int r = j / per;
-          const uint32_t w = reinterpret_cast<const uint32_t*>(
-              cluster.map_shared_rank(pub_scores, r))[g * per + (j - r * per)];
-          if (g < G) reinterpret_cast<uint32_t*>(es)[g * cap + j] = w;
-          else pages[j] = static_cast<int>(w);
+        const int items = CL * (G + 1) * nl;
+        for (int i = tid; i < items; i += Tr::kThreads) {
+          const int r = i / ((G + 1) * nl), k = i - r * (G + 1) * nl;
+          const int g = k / nl, jj = k - g * nl;
+          const uint32_t v = reinterpret_cast<const uint32_t*>(pub_scores)[g * per + jj];
+          uint32_t* dst = g < G ? reinterpret_cast<uint32_t*>(es + g * cap) : reinterpret_cast<uint32_t*>(pages);
+          cluster.map_shared_rank(dst, r)[lo + jj] = v;
         }
       }
       if (tid < CL * G) {
-        s_pm[tid] = pm;
-        s_pz[tid] = pz;
+        const int r = tid / G, g = tid - r * G;
+        cluster.map_shared_rank(s_pm, r)[rank * G + g] = pub.m[g];
+        cluster.map_shared_rank(s_pz, r)[rank * G + g] = pub.z[g];
       }
-      __syncthreads();
-      // per-head max and sum of exp over all n teams from the CL slices: warp g, lane r;
-      // s_gz holds 1 / (G z) so that p_j is a plain weighted sum
+      cluster.sync();                                                // barrier S1
+      // per-head max m and sum z over the CL slices (warp g, lane r), and the slice weights
+      // w_rg = exp(m_rg - m_g) / (G z_g), so that p_j = sum_g e_gj w_(r(j))g
       if (warp < G) {
         const float mr = lane < CL ? s_pm[lane * G + warp] : kNegInf;
         const float m = warp_max(mr);
-        const float zr = (lane < CL && mr != kNegInf) ? s_pz[lane * G + warp] * expf(mr - m) : 0.f;
-        const float z = warp_sum(zr);
-        if (lane == 0) {
-          s_gm[warp] = m;
-          s_gz[warp] = z > 0.f ? 1.f / (z * static_cast<float>(G)) : 0.f;
-        }
+        const float er = (lane < CL && mr != kNegInf) ? expf(mr - m) : 0.f;
+        const float z = warp_sum(lane < CL ? s_pz[lane * G + warp] * er : 0.f);
+        if (lane < CL) s_pm[lane * G + warp] = z > 0.f ? er / (z * static_cast<float>(G)) : 0.f;
       }
       __syncthreads();
-      // p_j = (1/G) sum_g exp(s_gj - m_g) / z_g, round(p_j 2^62) and the exact integer CDF:
-      // thread t takes teams [t*tpt, (t+1)*tpt), a serial sum, then one block-wide scan
+      // round(p_j 2^62) and the exact integer CDF: thread t takes teams [t*tpt, (t+1)*tpt),
+      // a serial sum, then one block-wide scan
       constexpr int kTpt = kMaxTeamsPerCta / Tr::kThreads;
       const int tpt = (n + Tr::kThreads - 1) / Tr::kThreads;          // <= kTpt
       const int jt = tid * tpt;
       const bool out_writer = writer && rank == 0;
       unsigned long long run = 0ull, incl_t[kTpt];
+      int rj = per > 0 ? jt / per : 0;                                // slice of team jt
 #pragma unroll
       for (int u = 0; u < kTpt; ++u) {
         const int j = jt + u;
         unsigned long long P = 0ull;
         if (u < tpt && j < n) {
+          if (j >= (rj + 1) * per) ++rj;
           float pj = 0.f;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float sc = es[g * cap + j];
-            pj += sc == kNegInf ? 0.f : expf(sc - s_gm[g]) * s_gz[g];
-          }
+          for (int g = 0; g < G; ++g) pj = fmaf(es[g * cap + j], s_pm[rj * G + g], pj);
           ps[j] = pj;
           flag[j] = 0;
           if (p.team_probs && out_writer) p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = pj;
@@ -493,7 +497,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         incl_t[u] = run;
       }
       unsigned long long Z;
-      const unsigned long long before = block_inclusive_scan<unsigned long long>(run, s_wd, Z) - run;
+      const unsigned long long before = block_exclusive_scan<unsigned long long>(run, s_wd, Z);
 #pragma unroll
       for (int u = 0; u < kTpt; ++u)
         if (u < tpt && jt + u < n) cdf[jt + u] = before + incl_t[u];
@@ -532,7 +536,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
       for (int u = 0; u < kTpt; ++u)
         if (valid && u < tpt && jt + u < n && flag[jt + u] == 1) ++mine;
       int count;
-      int k = block_inclusive_scan<int>(mine, s_wi, count) - mine;
+      int k = block_exclusive_scan<int>(mine, s_wi, count);
 #pragma unroll
       for (int u = 0; u < kTpt; ++u) {
         const int j = jt + u;
@@ -856,19 +860,23 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
     float o[kDT][4];
 #pragma unroll
     for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    // lr0, lr1: this lane's share of the running denominators (its own tokens), summed over
+    // the lanes of a head once after the loop
     float mr0 = kNegInf, mr1 = kNegInf, lr0 = 0.f, lr1 = 0.f;
-    int consumed = 0;
     const int mi = lane >> 3, lr = lane & 7;
-    for (int ci = 0; ci < n_chunks; ++ci) {
+    // One CTA barrier per chunk: each thread waits on the chunk's mbarrier itself; the
+    // barrier at the end of the chunk releases its stage and reports a timed-out wait, after
+    // which every thread leaves the loop together (the chunk's results are discarded).
+    bool timed_out = false;
+    int ci = 0;
+    for (; ci < n_chunks; ++ci) {
       const int stage = ci % S;
       if (!mbar_wait(&bar[stage], (ci / S) & 1)) {
         set_status(p.status, SANTA_DEV_TIMEOUT);
-        s_abort = 1;
+        timed_out = true;
       }
       const int vt = table[ci].valid;
       unsigned char* kst = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
-      __syncthreads();
-      if (s_abort) break;
       if (vt < kChunk) {                         // rows past the valid tokens: zero V (P = 0)
         unsigned char* vst = kst + Tr::kChunkBytes;
         for (int i = tid; i < (kChunk - vt) * 8 * (D / 64); i += Tr::kThreads) {
@@ -879,19 +887,21 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         fence_proxy_async_smem();  // before a later copy into this stage
         __syncthreads();
       }
-      consumed = ci + 1;
       const float lw2 = table[ci].lw2;
       const uint32_t kb = smem_u32(kst), vb = kb + Tr::kChunkBytes;
-      // scores of tokens r0, r0 + 8 for heads h0, h0 + 1
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      // scores of tokens r0, r0 + 8 for heads h0, h0 + 1 (even and odd k-steps in two
+      // accumulators: two dependent MMA chains of half the length)
+      float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kk = 0; kk < kKS; ++kk) {
         const int bx = (16 * kk) / 64, c0 = ((16 * kk) & 63) / 8;
         const int r = 16 * tile + lr + ((mi & 1) << 3), pc = c0 + (mi >> 1);
         uint32_t a[4];
         ldmatrix_x4(a, kb + bx * kBox + r * 128 + ((pc ^ (r & 7)) << 4));
-        mma_bf16_16816(c, a, qfrag[kk][0], qfrag[kk][1]);
+        mma_bf16_16816((kk & 1) ? c2 : c, a, qfrag[kk][0], qfrag[kk][1]);
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c[j] += c2[j];
       const bool t0ok = r0 < vt, t1ok = r0 + 8 < vt, g0ok = h0 < G, g1ok = h0 + 1 < G;
       const float s0 = (t0ok && g0ok) ? fmaf(c[0], p.scale_log2, lw2) : kNegInf;
       const float s1 = (t0ok && g1ok) ? fmaf(c[1], p.scale_log2, lw2) : kNegInf;
@@ -911,14 +921,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
       const float p1 = mn1 == kNegInf ? 0.f : exp2f(s1 - mn1);
       const float p2 = mn0 == kNegInf ? 0.f : exp2f(s2 - mn0);
       const float p3 = mn1 == kNegInf ? 0.f : exp2f(s3 - mn1);
-      float ps0 = p0 + p2, ps1 = p1 + p3;
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
-        ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
-      }
-      lr0 = fmaf(lr0, al0, ps0);
-      lr1 = fmaf(lr1, al1, ps1);
+      lr0 = fmaf(lr0, al0, p0 + p2);
+      lr1 = fmaf(lr1, al1, p1 + p3);
       mr0 = mn0;
       mr1 = mn1;
 #pragma unroll
@@ -944,19 +948,25 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
         mma_bf16_16816(o[t], a, bh0, bh1);
         mma_bf16_16816(o[t], a, bl0, bl1);
       }
-      __syncthreads();
+      if (__syncthreads_or(timed_out)) break;
       if (tid == 0 && ci + S < n_chunks) issue(ci + S);
     }
-    if (s_abort) {
-      // wait (bounded) for the copies still in flight; contribute nothing
+    if (ci < n_chunks) {
+      // a wait at chunk ci gave up: wait (bounded) for the copies that may still be in
+      // flight (chunks ci .. ci + S - 1), and contribute nothing
       if (tid == 0)
-        for (int ci = consumed; ci < min(consumed + S, n_chunks); ++ci)
-          (void)mbar_wait(&bar[ci % S], (ci / S) & 1);
+        for (int cj = ci; cj < min(ci + S, n_chunks); ++cj)
+          (void)mbar_wait(&bar[cj % S], (cj / S) & 1);
       mr0 = mr1 = kNegInf;
       lr0 = lr1 = 0.f;
 #pragma unroll
       for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
       __syncthreads();
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      lr0 += __shfl_xor_sync(0xffffffffu, lr0, off);
+      lr1 += __shfl_xor_sync(0xffffffffu, lr1, off);
     }
     if (attending) {
       // warp partials: O^T elements (d = d0 + lane/4 (+8), head h0 / h0 + 1), (m, l) per head
