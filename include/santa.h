@@ -192,7 +192,9 @@ int santa_attend(const santa_decode_args* a, void* stream);
  * santa_decode_plan — the launch the library would use for `a` (whose pointers need not be
  * valid; only shapes and workspace_bytes are read): out[0] = CTAs per thread-block cluster
  * (CL), out[1] = clusters per unit (NC; NC > 1 routes partials through the workspace),
- * out[2] = teams one CTA scores, out[3] = clusters of CL CTAs the device can run at once.
+ * out[2] = teams one CTA scores, out[3] = clusters of CL CTAs the device can run at once,
+ * out[4] = 1 if the wide variant runs (bf16 steps whose launch fits one CTA per SM: six
+ * stages, two warp groups consuming alternate chunks), else 0.  `out` holds 5 entries.
  * `which`: 0 santa_decode, 1 santa_sample, 2 santa_attend, 3 santa_dense_decode.
  */
 int santa_decode_plan(const santa_decode_args* a, int which, int32_t* out);

@@ -303,8 +303,9 @@ _PLAN_MODES = {"decode": 0, "sample": 1, "attend": 2, "dense": 3}
 
 def santa_decode_plan(q, k_pool, page_table, num_draws: int, which: str = "decode",
                       workspace_bytes: int | None = None) -> dict:
-    """The launch shape the library picks: cluster size, clusters per unit, teams per CTA
-    and the device's co-resident cluster count for that size."""
+    """The launch shape the library picks: cluster size, clusters per unit, teams per CTA,
+    the device's co-resident cluster count for that size, and whether the wide
+    (one-CTA-per-SM) variant runs."""
     B, Hq, d = q.shape
     _, Hkv, T, _ = k_pool.shape
     a = _DecodeArgs()
@@ -319,10 +320,10 @@ def santa_decode_plan(q, k_pool, page_table, num_draws: int, which: str = "decod
                                                         page_table.shape[1], num_draws))
     a.workspace = 256 if workspace_bytes else None        # only its size is read
     a.workspace_bytes = workspace_bytes
-    out = (ctypes.c_int32 * 4)()
+    out = (ctypes.c_int32 * 5)()
     _check(lib().santa_decode_plan(ctypes.byref(a), _PLAN_MODES[which], out), "santa_decode_plan")
     return {"cluster": out[0], "clusters_per_unit": out[1], "teams_per_cta": out[2],
-            "max_active_clusters": out[3]}
+            "max_active_clusters": out[3], "wide": bool(out[4])}
 
 
 def santa_noalloc_scratch_bytes() -> int:

@@ -57,6 +57,18 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
+// Barrier over `nthreads` threads (a multiple of 32) on named barrier `id` (1..15), which
+// returns whether `pred` held for any of them.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<int>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy (bulk
 // copy) accesses of the same bytes; a barrier must follow before the copy is issued.
 __device__ __forceinline__ void fence_proxy_async_smem() {

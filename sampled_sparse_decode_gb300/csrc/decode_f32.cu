@@ -7,21 +7,21 @@ namespace santa {
 cudaError_t decode_launch_f32(const DecodeParams& p, int head_dim, int group, dim3 grid,
                               int cluster, cudaStream_t stream) {
   if (head_dim == 128) {
-    SANTA_DISPATCH_G(group, return (decode_launch_t<false, 128, GG>(p, grid, cluster, stream)))
+    SANTA_DISPATCH_G(group, return (decode_launch_t<false, 128, GG, false>(p, grid, cluster, stream)))
   }
-  SANTA_DISPATCH_G(group, return (decode_launch_t<false, 64, GG>(p, grid, cluster, stream)))
+  SANTA_DISPATCH_G(group, return (decode_launch_t<false, 64, GG, false>(p, grid, cluster, stream)))
 }
 
 int decode_resident_f32(int head_dim, int group) {
-  if (head_dim == 128) { SANTA_DISPATCH_G(group, return (decode_resident_t<false, 128, GG>())) }
-  SANTA_DISPATCH_G(group, return (decode_resident_t<false, 64, GG>()))
+  if (head_dim == 128) { SANTA_DISPATCH_G(group, return (decode_resident_t<false, 128, GG, false>())) }
+  SANTA_DISPATCH_G(group, return (decode_resident_t<false, 64, GG, false>()))
 }
 
 int decode_max_clusters_f32(int head_dim, int group, int cluster) {
   if (head_dim == 128) {
-    SANTA_DISPATCH_G(group, return (decode_max_clusters_t<false, 128, GG>(cluster)))
+    SANTA_DISPATCH_G(group, return (decode_max_clusters_t<false, 128, GG, false>(cluster)))
   }
-  SANTA_DISPATCH_G(group, return (decode_max_clusters_t<false, 64, GG>(cluster)))
+  SANTA_DISPATCH_G(group, return (decode_max_clusters_t<false, 64, GG, false>(cluster)))
 }
 
 }  // namespace santa

@@ -72,14 +72,17 @@ struct Published {
   int pad;
 };
 
-template <bool BF16, int D, int G>
+template <bool BF16, int D, int G, bool W = false>
 struct DecodeTraits {
   static constexpr int kThreads = 256;
   static constexpr int kWarps = 8;
   static constexpr int kEsize = BF16 ? 2 : 4;
   static constexpr int kChunkBytes = kChunk * D * kEsize;
   static constexpr int kStageBytes = 2 * kChunkBytes;
-  static constexpr int kStages = kStageBytes >= 65536 ? 2 : (kStageBytes >= 32768 ? 3 : 4);
+  // W (wide): one CTA per SM, six stages, two warp groups consuming alternate chunks (each
+  // group owns the even or the odd stages); otherwise up to two CTAs per SM
+  static constexpr int kStages =
+      W ? 6 : (kStageBytes >= 65536 ? 2 : (kStageBytes >= 32768 ? 3 : 4));
   static constexpr int kEplS = D / 16;
   static constexpr int kEplV = D / 32;
   static constexpr int kRing = kStages * kStageBytes;
@@ -112,7 +115,8 @@ struct DecodeTraits {
   static constexpr size_t kAOff = kPOff + sizeof(float) * kWarps * 64;
   static constexpr size_t kBarOff = kAOff + sizeof(float) * kWarps * kMaxGroup;
   static constexpr size_t kSmem = kBarOff + sizeof(uint64_t) * kStages;
-  static constexpr int kMinBlocks = kSmem <= 112 * 1024 ? 2 : 1;
+  static constexpr int kMinBlocks = (!W && kSmem <= 112 * 1024) ? 2 : 1;
+  static_assert(!W || (BF16 && kStages % 2 == 0), "wide: bf16 only, even stage count");
 };
 
 // ---------------------------------------------------------------- element loaders
@@ -304,10 +308,10 @@ __device__ __forceinline__ void score_teams(const DecodeParams& p, int b, int h,
 
 // ---------------------------------------------------------------- the kernel
 
-template <bool BF16, int D, int G>
-__global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
+template <bool BF16, int D, int G, bool W>
+__global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks))
     decode_kernel(const __grid_constant__ DecodeParams p) {
-  using Tr = DecodeTraits<BF16, D, G>;
+  using Tr = DecodeTraits<BF16, D, G, W>;
   constexpr int S = Tr::kStages;
   constexpr float kNegInf = -INFINITY;
   cgx::cluster_group cluster = cgx::this_cluster();
@@ -833,7 +837,177 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
   float* part = reinterpret_cast<float*>(smem) + Tr::kPartialOff;    // acc [G][D], m [8], l [8]
   float* part_m = part + G * D;
   float* part_l = part_m + kMaxGroup;
-  if constexpr (BF16) {
+  if constexpr (BF16 && W) {
+    // ---- bf16 K/V, wide variant: warp group grp = warp >> 2 consumes chunks ci = grp,
+    // grp + 2, ... (the stage count is even, so each group owns its stages and refills them
+    // itself); warp (grp, tile) computes the scores of its 16-token tile and P.V over all
+    // of d.  Same fragments, swizzle and P hi/lo split as the two-CTA variant below.
+    constexpr int kKS = D / 16;                  // k-steps of the scores
+    constexpr int kDT = D / 16;                  // 16-row d-tiles (all of d)
+    constexpr int kBox = kChunk * 128;           // bytes of one 64-row box
+    const int grp = warp >> 2, tile = warp & 3, gtid = tid & 127;
+    const int h0 = 2 * (lane & 3);               // this lane's heads h0, h0 + 1
+    const int r0 = 16 * tile + (lane >> 2);      // this lane's tokens r0, r0 + 8
+    uint32_t qfrag[kKS][2];
+    {
+      const int n = lane >> 2, kq = 2 * (lane & 3);
+      const uint16_t* qh = static_cast<const uint16_t*>(p.q) +
+                           (static_cast<int64_t>(b) * p.num_q_heads + h * G + (n < G ? n : 0)) * D;
+#pragma unroll
+      for (int kk = 0; kk < kKS; ++kk) {
+        qfrag[kk][0] = n < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + kq) : 0u;
+        qfrag[kk][1] = n < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + kq) : 0u;
+      }
+    }
+    float o[kDT][4];
+#pragma unroll
+    for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    float mr0 = kNegInf, mr1 = kNegInf, lr0 = 0.f, lr1 = 0.f;   // lr: this lane's share
+    const int mi = lane >> 3, lr = lane & 7;
+    bool timed_out = false;
+    int ci = grp;
+    for (; ci < n_chunks; ci += 2) {
+      const int stage = ci % S;
+      if (!mbar_wait(&bar[stage], (ci / S) & 1)) {
+        set_status(p.status, SANTA_DEV_TIMEOUT);
+        timed_out = true;
+      }
+      const int vt = table[ci].valid;
+      unsigned char* kst = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
+      if (vt < kChunk) {                         // rows past the valid tokens: zero V (P = 0)
+        unsigned char* vst = kst + Tr::kChunkBytes;
+        for (int i = gtid; i < (kChunk - vt) * 8 * (D / 64); i += 128) {
+          const int bx = i / ((kChunk - vt) * 8), rem = i - bx * (kChunk - vt) * 8;
+          const int row = vt + rem / 8, piece = rem & 7;
+          *reinterpret_cast<uint4*>(vst + bx * kBox + row * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();                // before a later copy into this stage
+        bar_red_or(1 + grp, 128, false);
+      }
+      const float lw2 = table[ci].lw2;
+      const uint32_t kb = smem_u32(kst), vb = kb + Tr::kChunkBytes;
+      float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < kKS; ++kk) {
+        const int bx = (16 * kk) / 64, c0 = ((16 * kk) & 63) / 8;
+        const int r = 16 * tile + lr + ((mi & 1) << 3), pc = c0 + (mi >> 1);
+        uint32_t a[4];
+        ldmatrix_x4(a, kb + bx * kBox + r * 128 + ((pc ^ (r & 7)) << 4));
+        mma_bf16_16816((kk & 1) ? c2 : c, a, qfrag[kk][0], qfrag[kk][1]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c[j] += c2[j];
+      const bool t0ok = r0 < vt, t1ok = r0 + 8 < vt, g0ok = h0 < G, g1ok = h0 + 1 < G;
+      const float s0 = (t0ok && g0ok) ? fmaf(c[0], p.scale_log2, lw2) : kNegInf;
+      const float s1 = (t0ok && g1ok) ? fmaf(c[1], p.scale_log2, lw2) : kNegInf;
+      const float s2 = (t1ok && g0ok) ? fmaf(c[2], p.scale_log2, lw2) : kNegInf;
+      const float s3 = (t1ok && g1ok) ? fmaf(c[3], p.scale_log2, lw2) : kNegInf;
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
+      const float al0 = mn0 == kNegInf ? 1.f : exp2f(mr0 - mn0);
+      const float al1 = mn1 == kNegInf ? 1.f : exp2f(mr1 - mn1);
+      const float p0 = mn0 == kNegInf ? 0.f : exp2f(s0 - mn0);
+      const float p1 = mn1 == kNegInf ? 0.f : exp2f(s1 - mn1);
+      const float p2 = mn0 == kNegInf ? 0.f : exp2f(s2 - mn0);
+      const float p3 = mn1 == kNegInf ? 0.f : exp2f(s3 - mn1);
+      lr0 = fmaf(lr0, al0, p0 + p2);
+      lr1 = fmaf(lr1, al1, p1 + p3);
+      mr0 = mn0;
+      mr1 = mn1;
+#pragma unroll
+      for (int t = 0; t < kDT; ++t) {
+        o[t][0] *= al0;
+        o[t][1] *= al1;
+        o[t][2] *= al0;
+        o[t][3] *= al1;
+      }
+      const uint32_t hi01 = pack_bf16(p0, p1), hi23 = pack_bf16(p2, p3);
+      const uint32_t lo01 = pack_bf16(p0 - bf16_lo_f(hi01), p1 - bf16_hi_f(hi01));
+      const uint32_t lo23 = pack_bf16(p2 - bf16_lo_f(hi23), p3 - bf16_hi_f(hi23));
+      const uint32_t bh0 = movmatrix_trans(hi01), bh1 = movmatrix_trans(hi23);
+      const uint32_t bl0 = movmatrix_trans(lo01), bl1 = movmatrix_trans(lo23);
+#pragma unroll
+      for (int t = 0; t < kDT; ++t) {
+        const int d0 = 16 * t;
+        const int bx = d0 / 64, cd = (d0 & 63) / 8;
+        const int r = 16 * tile + lr + ((mi >> 1) << 3), pc = cd + (mi & 1);
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, vb + bx * kBox + r * 128 + ((pc ^ (r & 7)) << 4));
+        mma_bf16_16816(o[t], a, bh0, bh1);
+        mma_bf16_16816(o[t], a, bl0, bl1);
+      }
+      // the group's barrier releases the stage (and reports a timed-out wait)
+      if (bar_red_or(1 + grp, 128, timed_out)) break;
+      if (gtid == 0 && ci + S < n_chunks) issue(ci + S);
+    }
+    if (ci < n_chunks) {
+      // a wait of this group gave up at chunk ci: wait (bounded) for the group's copies that
+      // may still be in flight (ci, ci + 2, .. below ci + S), and flag the CTA
+      if (gtid == 0)
+        for (int cj = ci; cj < min(ci + S, n_chunks); cj += 2)
+          (void)mbar_wait(&bar[cj % S], (cj / S) & 1);
+      s_abort = 1;
+    }
+    __syncthreads();                             // both groups done with the ring
+    if (s_abort) {
+      mr0 = mr1 = kNegInf;
+      lr0 = lr1 = 0.f;
+#pragma unroll
+      for (int t = 0; t < kDT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      lr0 += __shfl_xor_sync(0xffffffffu, lr0, off);
+      lr1 += __shfl_xor_sync(0xffffffffu, lr1, off);
+    }
+    if (attending) {
+      // warp partials over all of d; every warp has its own (m, l) per head
+#pragma unroll
+      for (int t = 0; t < kDT; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int d = 16 * t + (lane >> 2) + ((j >> 1) << 3);
+          const int g = h0 + (j & 1);
+          if (g < G) mrg_acc[(warp * G + g) * D + d] = o[t][j];
+        }
+      if (lane < 4) {
+        mrg_m[warp * kMaxGroup + h0] = mr0;
+        mrg_m[warp * kMaxGroup + h0 + 1] = mr1;
+        mrg_l[warp * kMaxGroup + h0] = lr0;
+        mrg_l[warp * kMaxGroup + h0 + 1] = lr1;
+      }
+      __syncthreads();
+      if (tid < G) {
+        float mx = kNegInf;
+#pragma unroll
+        for (int w = 0; w < Tr::kWarps; ++w) mx = fmaxf(mx, mrg_m[w * kMaxGroup + tid]);
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < Tr::kWarps; ++w) {
+          const float mw = mrg_m[w * kMaxGroup + tid];
+          const float wt = mw == kNegInf ? 0.f : exp2f(mw - mx);
+          arow[w * kMaxGroup + tid] = wt;
+          l = fmaf(wt, mrg_l[w * kMaxGroup + tid], l);
+        }
+        part_m[tid] = mx;
+        part_l[tid] = l;
+      }
+      __syncthreads();
+      for (int i = tid; i < G * D; i += Tr::kThreads) {
+        const int g = i / D, k = i - g * D;
+        float a = 0.f;
+#pragma unroll
+        for (int w = 0; w < Tr::kWarps; ++w)
+          a = fmaf(arow[w * kMaxGroup + g], mrg_acc[(w * G + g) * D + k], a);
+        part[i] = a;
+      }
+    }
+  } else if constexpr (BF16) {
     // ---- bf16 K/V: tensor-core scores and P.V (mma.sync m16n8k16, fp32 accumulate)
     // Warp w owns 16-token tile (w & 3) of every chunk for the scores S^T = K Q^T (the G <= 8
     // heads are the N = 8 dimension) and half (w >> 2) of d for O^T += V^T P^T.  The chunk's
@@ -1279,18 +1453,18 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G>::kMinBlocks))
 
 // ---------------------------------------------------------------- host-side launch helpers
 
-template <bool BF16, int D, int G>
+template <bool BF16, int D, int G, bool W>
 std::atomic<unsigned long long>& decode_smem_flag() {
   static std::atomic<unsigned long long> flag{0};
   return flag;
 }
 
-template <bool BF16, int D, int G>
+template <bool BF16, int D, int G, bool W>
 cudaError_t decode_prepare_t() {
-  using Tr = DecodeTraits<BF16, D, G>;
-  auto* kern = decode_kernel<BF16, D, G>;
+  using Tr = DecodeTraits<BF16, D, G, W>;
+  auto* kern = decode_kernel<BF16, D, G, W>;
   static std::atomic<unsigned long long> cluster_flag{0};
-  cudaError_t e = ensure_dynamic_smem(kern, Tr::kSmem, decode_smem_flag<BF16, D, G>());
+  cudaError_t e = ensure_dynamic_smem(kern, Tr::kSmem, decode_smem_flag<BF16, D, G, W>());
   if (e != cudaSuccess) return e;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1304,10 +1478,10 @@ cudaError_t decode_prepare_t() {
 }
 
 // How many clusters of `cluster` CTAs can be co-resident (0 if none / on error).
-template <bool BF16, int D, int G>
+template <bool BF16, int D, int G, bool W>
 int decode_max_clusters_t(int cluster) {
-  using Tr = DecodeTraits<BF16, D, G>;
-  if (decode_prepare_t<BF16, D, G>() != cudaSuccess) return 0;
+  using Tr = DecodeTraits<BF16, D, G, W>;
+  if (decode_prepare_t<BF16, D, G, W>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, 1, 1);
   cfg.blockDim = dim3(Tr::kThreads);
@@ -1320,26 +1494,26 @@ int decode_max_clusters_t(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<BF16, D, G>, &cfg) != cudaSuccess)
+  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<BF16, D, G, W>, &cfg) != cudaSuccess)
     return 0;
   return n;
 }
 
-template <bool BF16, int D, int G>
+template <bool BF16, int D, int G, bool W>
 int decode_resident_t() {
-  using Tr = DecodeTraits<BF16, D, G>;
-  if (decode_prepare_t<BF16, D, G>() != cudaSuccess) return 0;
+  using Tr = DecodeTraits<BF16, D, G, W>;
+  if (decode_prepare_t<BF16, D, G, W>() != cudaSuccess) return 0;
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, decode_kernel<BF16, D, G>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, decode_kernel<BF16, D, G, W>,
                                                     Tr::kThreads, Tr::kSmem) != cudaSuccess)
     return 0;
   return blocks;
 }
 
-template <bool BF16, int D, int G>
+template <bool BF16, int D, int G, bool W>
 cudaError_t decode_launch_t(const DecodeParams& p, dim3 grid, int cluster, cudaStream_t stream) {
-  using Tr = DecodeTraits<BF16, D, G>;
-  cudaError_t e = decode_prepare_t<BF16, D, G>();
+  using Tr = DecodeTraits<BF16, D, G, W>;
+  cudaError_t e = decode_prepare_t<BF16, D, G, W>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -1353,7 +1527,7 @@ cudaError_t decode_launch_t(const DecodeParams& p, dim3 grid, int cluster, cudaS
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<BF16, D, G>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<BF16, D, G, W>, p);
 }
 
 // Dispatch on the group size (1..8) for one (dtype, head_dim).

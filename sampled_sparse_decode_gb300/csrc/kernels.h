@@ -69,5 +69,10 @@ int decode_resident_bf16(int head_dim, int group);
 int decode_resident_f32(int head_dim, int group);
 int decode_max_clusters_bf16(int head_dim, int group, int cluster);
 int decode_max_clusters_f32(int head_dim, int group, int cluster);
+// wide variant (bf16 only): one CTA per SM, six stages, two warp groups
+cudaError_t decode_launch_bf16_wide(const DecodeParams& p, int head_dim, int group, dim3 grid,
+                                    int cluster, cudaStream_t stream);
+int decode_resident_bf16_wide(int head_dim, int group);
+int decode_max_clusters_bf16_wide(int head_dim, int group, int cluster);
 
 }  // namespace santa

@@ -109,29 +109,33 @@ int pow2_at_least(int64_t x) {
   return c;
 }
 
-int resident_ctas(bool bf16, int d, int G) {
+// CTAs of the kernel one SM holds; `wide` selects the one-CTA-per-SM bf16 variant.
+int resident_ctas(bool bf16, int d, int G, bool wide) {
   static std::mutex mu;
-  static int cache[64][2][2][santa::kMaxGroup + 1] = {};
+  static int cache[64][2][2][2][santa::kMaxGroup + 1] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  int& c = cache[dev][bf16][d == 128][G];
-  if (!c) c = bf16 ? santa::decode_resident_bf16(d, G) : santa::decode_resident_f32(d, G);
+  int& c = cache[dev][bf16][wide][d == 128][G];
+  if (!c)
+    c = bf16 ? (wide ? santa::decode_resident_bf16_wide(d, G) : santa::decode_resident_bf16(d, G))
+             : santa::decode_resident_f32(d, G);
   return c;
 }
 
 // Clusters of `cl` CTAs the device can run at once (cached per device and shape).
-int max_clusters(bool bf16, int d, int G, int cl) {
+int max_clusters(bool bf16, int d, int G, int cl, bool wide) {
   static std::mutex mu;
-  static int cache[64][2][2][santa::kMaxGroup + 1][5] = {};  // 0 unknown, -1 none
+  static int cache[64][2][2][2][santa::kMaxGroup + 1][5] = {};  // 0 unknown, -1 none
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   int li = 0;
   while ((1 << li) < cl) ++li;
   std::lock_guard<std::mutex> lock(mu);
-  int& c = cache[dev][bf16][d == 128][G][li];
+  int& c = cache[dev][bf16][wide][d == 128][G][li];
   if (!c) {
-    const int n = bf16 ? santa::decode_max_clusters_bf16(d, G, cl)
+    const int n = bf16 ? (wide ? santa::decode_max_clusters_bf16_wide(d, G, cl)
+                               : santa::decode_max_clusters_bf16(d, G, cl))
                        : santa::decode_max_clusters_f32(d, G, cl);
     c = n > 0 ? n : -1;
   }
@@ -142,6 +146,7 @@ struct Plan {
   int cluster = 1;       // CL
   int clusters = 1;      // NC
   int tpc = 1;           // teams per CTA in the sampling phase
+  bool wide = false;     // bf16 one-CTA-per-SM variant
   uint32_t* counters = nullptr;
   float* part_ml = nullptr;
   float* part_acc = nullptr;
@@ -149,10 +154,10 @@ struct Plan {
 
 // Chooses CL and NC for a shape; nc_cap limits NC (the workspace's capacity).
 int choose(int dtype, int64_t units, int G, int d, int T, int max_teams, int M, int mode,
-           int64_t nc_cap, Plan* pl) {
+           int64_t nc_cap, bool wide, Plan* pl) {
   const bool bf16 = dtype == SANTA_BF16;
   const int sms = current_sms();
-  const int res = resident_ctas(bf16, d, G);
+  const int res = resident_ctas(bf16, d, G, wide);
   if (sms <= 0 || res <= 0) return SANTA_ERR_CUDA;
   const int64_t slots = static_cast<int64_t>(sms) * res;
   const int64_t spu = std::max<int64_t>(1, slots / units);
@@ -176,7 +181,7 @@ int choose(int dtype, int64_t units, int G, int d, int T, int max_teams, int M, 
   int cl = -1;
   int64_t nc = 1;
   for (int c = cl_start; c >= cl_lo; c >>= 1) {
-    const int maxc = max_clusters(bf16, d, G, c);
+    const int maxc = max_clusters(bf16, d, G, c, wide);
     if (maxc <= 0) continue;
     const int64_t nc_min = cmax > 0 ? ceil_div(cmax, static_cast<int64_t>(santa::kMaxChunksPerSplit) * c) : 1;
     if (nc_min > nc_limit) continue;
@@ -194,6 +199,23 @@ int choose(int dtype, int64_t units, int G, int d, int T, int max_teams, int M, 
   pl->cluster = cl;
   pl->clusters = static_cast<int>(nc);
   pl->tpc = static_cast<int>(std::max<int64_t>(1, ceil_div(max_teams, cl)));
+  pl->wide = wide;
+  return SANTA_OK;
+}
+
+// The two-CTA-per-SM plan, replaced by the wide variant's plan when the step is a bf16
+// attending one and both plans need no more CTAs than the device has SMs (each CTA then has
+// an SM to itself anyway, and the wide variant consumes two chunks at a time).
+int choose_variant(int dtype, int64_t units, int G, int d, int T, int max_teams, int M,
+                   int mode, int64_t nc_cap, Plan* pl) {
+  int rc = choose(dtype, units, G, d, T, max_teams, M, mode, nc_cap, false, pl);
+  if (rc || dtype != SANTA_BF16 || mode == santa::kModeSample) return rc;
+  const int64_t sms = current_sms();
+  if (units * pl->cluster * pl->clusters > sms) return SANTA_OK;
+  Plan w;
+  if (choose(dtype, units, G, d, T, max_teams, M, mode, nc_cap, true, &w) == SANTA_OK &&
+      units * w.cluster * w.clusters <= sms)
+    *pl = w;
   return SANTA_OK;
 }
 
@@ -211,8 +233,8 @@ int make_plan(const santa_decode_args* a, int mode, Plan* pl) {
       nc_cap = std::max<int64_t>(1, static_cast<int64_t>((a->workspace_bytes - fixed) /
                                                          cluster_partial_bytes(units, G, d)));
   }
-  int rc = choose(a->dtype, units, G, d, a->team_size, a->max_teams, a->num_draws, mode, nc_cap,
-                  pl);
+  int rc = choose_variant(a->dtype, units, G, d, a->team_size, a->max_teams, a->num_draws, mode,
+                          nc_cap, pl);
   if (rc) return rc;
   if (pl->clusters > 1) {
     if (!base) return SANTA_ERR_INVALID_ARG;
@@ -232,7 +254,8 @@ size_t default_ws_bytes(int dtype, int batch, int hq, int hkv, int d, int T, int
   if (mode != santa::kModeDense && (M < 1 || M > kMaxDraws)) return 0;
   Plan pl;
   const int64_t units = static_cast<int64_t>(batch) * hkv;
-  if (choose(dtype, units, hq / hkv, d, T, max_teams, M, mode, santa::kMaxClustersPerUnit, &pl))
+  if (choose_variant(dtype, units, hq / hkv, d, T, max_teams, M, mode,
+                     santa::kMaxClustersPerUnit, &pl))
     return 0;
   return ws_bytes_for(units, hq / hkv, d, pl.clusters);
 }
@@ -323,7 +346,8 @@ int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   const int G = a->num_q_heads / a->num_kv_heads;
   const cudaError_t e =
       a->dtype == SANTA_BF16
-          ? santa::decode_launch_bf16(p, a->head_dim, G, grid, pl.cluster, stream)
+          ? (pl.wide ? santa::decode_launch_bf16_wide(p, a->head_dim, G, grid, pl.cluster, stream)
+                     : santa::decode_launch_bf16(p, a->head_dim, G, grid, pl.cluster, stream))
           : santa::decode_launch_f32(p, a->head_dim, G, grid, pl.cluster, stream);
   return map_cuda(e);
 }
@@ -429,7 +453,8 @@ int santa_decode_plan(const santa_decode_args* a, int which, int32_t* out) {
   out[1] = pl.clusters;
   out[2] = pl.tpc;
   out[3] = max_clusters(a->dtype == SANTA_BF16, a->head_dim, a->num_q_heads / a->num_kv_heads,
-                        pl.cluster);
+                        pl.cluster, pl.wide);
+  out[4] = pl.wide ? 1 : 0;
   return SANTA_OK;
 }
 

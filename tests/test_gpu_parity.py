@@ -37,6 +37,9 @@ SMALL = {
     # one long sequence, one KV head: dense work spans several clusters
     "long_b1_multicluster": dict(cfg="long_128k_b4_m64", batch=1, q_heads=7, kv_heads=1,
                                  seq_len=40000, draws=600, num_pages=0),
+    # 160 units: more CTAs than SMs, so bf16 steps take the two-CTA-per-SM variant (the
+    # smaller cases take the wide one-CTA-per-SM variant)
+    "qwen_b40_two_per_sm": dict(cfg="qwen7b_32k_b8_m64", batch=40, seq_len=1300),
     # 4096 draws over 4096 teams: more chunks than one cluster's tables hold, so the sampled
     # step itself spans two clusters (partials through the workspace)
     "f32_b1_two_clusters": dict(cfg="tiny_f32", seq_len=4096 * 128, team_size=128,
@@ -51,6 +54,18 @@ def test_multicluster_cases_take_the_multicluster_path():
         dw = DeviceWorkload(wl)
         plan = santa.santa_decode_plan(dw.q, dw.k_pool, dw.page_table, wl.cfg.draws, which)
         assert plan["clusters_per_unit"] >= 2, (name, which, plan)
+
+
+def test_both_kernel_variants_are_covered():
+    for name, want in [("qwen_b2_ragged", True), ("bf16_d64_t64", True),
+                       ("qwen_b40_two_per_sm", False)]:
+        wl = make(SMALL[name])
+        dw = DeviceWorkload(wl)
+        for which in ("decode", "attend", "dense"):
+            plan = santa.santa_decode_plan(dw.q, dw.k_pool, dw.page_table, wl.cfg.draws, which)
+            assert plan["wide"] == want, (name, which, plan)
+        assert not santa.santa_decode_plan(dw.q, dw.k_pool, dw.page_table, wl.cfg.draws,
+                                           "sample")["wide"]
 
 
 def make(spec, **extra):
