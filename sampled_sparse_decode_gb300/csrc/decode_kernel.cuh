@@ -247,6 +247,36 @@ __device__ __forceinline__ V block_exclusive_scan(V v, V* warp_tot, V& total) {
   return pre + incl - v;
 }
 
+// Team of sampled slot k (0-based, k < the number of set bits): the k-th set bit of the
+// team mask, whose 32-bit words are grouped in 8 runs of `wpw` words with set-bit counts
+// gtot[0..7].  Slots follow ascending team order.
+__device__ __forceinline__ int select_team(const uint32_t* mask, const int* gtot, int wpw, int k) {
+  int g = 0;
+  while (g < 7 && k >= gtot[g]) k -= gtot[g++];
+  int w = g * wpw;
+  for (;;) {
+    const int c = __popc(mask[w]);
+    if (k < c) break;
+    k -= c;
+    ++w;
+  }
+  uint32_t m = mask[w];
+  int pos = 0;
+#pragma unroll
+  for (int half = 16; half; half >>= 1) {
+    const uint32_t lo = m & ((1u << half) - 1u);
+    const int c = __popc(lo);
+    if (k >= c) {
+      k -= c;
+      m >>= half;
+      pos += half;
+    } else {
+      m = lo;
+    }
+  }
+  return 32 * w + pos;
+}
+
 // Scores s_{g,j} = q_g . rep_j / sqrt(d) of teams [t0, t0 + cnt) of unit (b, h), written
 // to es[g * stride + j] (j relative to t0); pg[j] receives the team's page id, or -2 for a
 // page id out of range (score -inf, status bit).  The page ids of a batch are read in one
@@ -377,6 +407,9 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   const bool local = (G + 1) * per <= kPubScores && n <= kMaxTeamsPerCta;
   ListEntry* llist = nullptr;             // local sampling: the drawn teams, in slot order
   const int* lpages = nullptr;            // local sampling: page id of every team of the unit
+  const uint32_t* lmask = nullptr;        // local sampling: bit mask of the drawn teams
+  const float* lps = nullptr;             // local sampling: team probabilities
+  int lwpw = 1;                           // local sampling: mask words per warp
   if (sampling) {
     const int cap = local ? (max(n, 1) + 3) / 4 * 4 : p.teams_per_cta;   // rows 16-byte aligned
     unsigned long long* cdf = reinterpret_cast<unsigned long long*>(smem);   // [cap]
@@ -532,36 +565,27 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         for (int r = tid; r < M; r += Tr::kThreads) p.draw_ids[static_cast<int64_t>(unit) * M + r] = -1;
       }
       __syncthreads();
-      // the distinct drawn teams in ascending order, with pi and -log2 pi (same team split
-      // over threads as the CDF, one block-wide scan)
-      const float Mf = static_cast<float>(M);
-      int mine = 0;
-#pragma unroll
-      for (int u = 0; u < kTpt; ++u)
-        if (valid && u < tpt && jt + u < n && flag[jt + u] == 1) ++mine;
-      int count;
-      int k = block_exclusive_scan<int>(mine, s_wi, count);
-#pragma unroll
-      for (int u = 0; u < kTpt; ++u) {
-        const int j = jt + u;
-        if (valid && u < tpt && j < n && flag[j] == 1) {
-          const float piv = -expm1f(Mf * log1pf(-ps[j]));
-          llist[k] = ListEntry{j, -log2f(piv)};
-          if (out_writer) {
-            p.sel_ids[static_cast<int64_t>(unit) * M + k] = j;
-            p.pi[static_cast<int64_t>(unit) * M + k] = piv;
-          }
-          ++k;
+      // the distinct drawn teams as a bit mask over the teams (slot k = k-th set bit, so
+      // slots follow ascending team order): warp w ballots its run of wpw words
+      {
+        const int nw = (n + 31) / 32, wpw = (nw + 7) / 8;
+        uint32_t* mask = reinterpret_cast<uint32_t*>(llist);         // [nw]
+        int cnt = 0;
+        for (int w = warp * wpw; w < min(nw, (warp + 1) * wpw); ++w) {
+          const int j = 32 * w + lane;
+          const uint32_t bits = __ballot_sync(0xffffffffu, valid && j < n && flag[j] == 1);
+          if (lane == 0) mask[w] = bits;
+          cnt += __popc(bits);
         }
-      }
-      if (out_writer) {
-        for (int sidx = count + tid; sidx < M; sidx += Tr::kThreads) {
-          p.sel_ids[static_cast<int64_t>(unit) * M + sidx] = -1;
-          p.pi[static_cast<int64_t>(unit) * M + sidx] = 0.f;
-        }
-        if (tid == 0) p.sel_count[unit] = count;
+        if (lane == 0) s_wi[warp] = cnt;
+        lmask = mask;
+        lps = ps;
+        lwpw = wpw;
       }
       __syncthreads();
+      int count = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) count += s_wi[w];
       total_sel = count;
     } else {
       score_teams<D, G>(p, b, h, lo, nl, qs, rows, rows_cap, es, cap, flag);
@@ -756,6 +780,21 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   const int cps = (total_chunks + ctas - 1) / ctas;
   const int c_begin = min(gidx * cps, total_chunks);
   const int n_chunks = min(total_chunks - c_begin, cps);
+  const float Mf = static_cast<float>(M);
+  if (lmask && writer && rank == 0) {
+    // the sampling outputs of the unit: S in ascending order with pi, padded
+    for (int k = tid; k < M; k += Tr::kThreads) {
+      int team = -1;
+      float piv = 0.f;
+      if (k < total_sel) {
+        team = select_team(lmask, s_wi, lwpw, k);
+        piv = -expm1f(Mf * log1pf(-lps[team]));
+      }
+      p.sel_ids[static_cast<int64_t>(unit) * M + k] = team;
+      p.pi[static_cast<int64_t>(unit) * M + k] = piv;
+    }
+    if (tid == 0) p.sel_count[unit] = total_sel;
+  }
   for (int ci = tid; ci < n_chunks; ci += Tr::kThreads) {
     const int c = c_begin + ci;
     const int slot = c / cpt, part = c - slot * cpt;
@@ -765,7 +804,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     if (mode == kModeDecode) {
       ListEntry e;
       if (local) {
-        e = llist[slot];
+        e.team = select_team(lmask, s_wi, lwpw, slot);
+        e.lw2 = -log2f(-expm1f(Mf * log1pf(-lps[e.team])));
       } else {
         int owner = 0;
         while (owner + 1 < CL && s_base[owner + 1] <= slot) ++owner;
