@@ -72,6 +72,11 @@ def lib():
             "oracle_attend": (i32, [P, i32, i32, vp, vp, i32, vp]),
             "oracle_dense": (i32, [P, i32, i32, vp]),
             "oracle_decode": (i32, [P, vp, i32, u64, i32, i32, vp, vp, vp, vp, vp]),
+            "oracle_mix": (None, [vp, i32, dbl, vp]),
+            "oracle_systematic_point": (u64, [u64, i32, i32, u64]),
+            "oracle_draw_systematic": (None, [vp, i32, i32, u64, i32, i32, vp, vp, vp]),
+            "oracle_select_ex": (i32, [vp, i32, vp, i32, i32, vp, vp]),
+            "oracle_decode_ex": (i32, [P, vp, i32, u64, i32, i32, i32, dbl, vp, vp, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -240,3 +245,61 @@ def decode(pr: Problem, reps: np.ndarray, M: int, seed: int, b: int, h: int) -> 
                                      _ptr(draws), _ptr(sel), _ptr(pi), _ptr(p), _ptr(out)),
                  "decode")
     return UnitResult(draws, sel[:cnt].copy(), pi[:cnt].copy(), p[:pr.n_teams(b)].copy(), out)
+
+
+# ---------------------------------------------------------------- sampler variants
+
+SAMPLERS = {"iid_ht": 0, "systematic": 1, "iid_hh": 2}
+
+
+def mix(p: np.ndarray, alpha: float) -> np.ndarray:
+    """Defensive mixture q = (1 - alpha) p + alpha / n."""
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    q = np.zeros_like(p)
+    lib().oracle_mix(_ptr(p), p.size, float(alpha), _ptr(q))
+    return q
+
+
+def systematic_point(t_u: int, r: int, M: int, Z: int) -> int:
+    return int(lib().oracle_systematic_point(int(t_u), int(r), int(M), int(Z)))
+
+
+def draw_systematic(q: np.ndarray, M: int, seed: int, b: int, h: int):
+    """Returns (draws [M] int32, t [M] uint64, C [n] uint64) for the systematic sampler."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    n = q.size
+    draws = np.zeros(M, dtype=np.int32)
+    t = np.zeros(M, dtype=np.uint64)
+    C = np.zeros(n, dtype=np.uint64)
+    lib().oracle_draw_systematic(_ptr(q), n, M, seed, b, h, _ptr(draws), _ptr(t), _ptr(C))
+    return draws, t, C
+
+
+def draw_with(sampler: str, q: np.ndarray, M: int, seed: int, b: int, h: int):
+    return draw_systematic(q, M, seed, b, h) if sampler == "systematic" else draw(q, M, seed, b, h)
+
+
+def select_ex(draws: np.ndarray, q: np.ndarray, sampler: str):
+    """Returns (sel ascending int32, recip = 1 / weight float64)."""
+    draws = np.ascontiguousarray(draws, dtype=np.int32)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    sel = np.zeros(max(draws.size, 1), dtype=np.int32)
+    rc = np.zeros(max(draws.size, 1), dtype=np.float64)
+    cnt = _check(lib().oracle_select_ex(_ptr(draws), draws.size, _ptr(q), q.size,
+                                        SAMPLERS[sampler], _ptr(sel), _ptr(rc)), "select_ex")
+    return sel[:cnt].copy(), rc[:cnt].copy()
+
+
+def decode_ex(pr: Problem, reps: np.ndarray, M: int, seed: int, b: int, h: int,
+              sampler: str = "iid_ht", alpha: float = 0.0) -> UnitResult:
+    """One unit's decode step with a sampler variant and defensive mixture; UnitResult.p
+    holds the sampling distribution q and UnitResult.pi the 1 / weight of each team."""
+    draws = np.zeros(M, dtype=np.int32)
+    sel = np.zeros(M, dtype=np.int32)
+    rc = np.zeros(M, dtype=np.float64)
+    q = np.zeros(pr.max_teams, dtype=np.float64)
+    out = np.zeros((pr.G, pr.d), dtype=np.float64)
+    cnt = _check(lib().oracle_decode_ex(ctypes.byref(pr._c), _ptr(reps), M, seed, b, h,
+                                        SAMPLERS[sampler], float(alpha), _ptr(draws), _ptr(sel),
+                                        _ptr(rc), _ptr(q), _ptr(out)), "decode_ex")
+    return UnitResult(draws, sel[:cnt].copy(), rc[:cnt].copy(), q[:pr.n_teams(b)].copy(), out)

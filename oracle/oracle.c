@@ -272,6 +272,89 @@ int oracle_select(const int32_t* draws, int M, const double* p, int n, int32_t* 
   return count;
 }
 
+/* ---------------------------------------------------------------- sampler variants */
+
+/*
+ * Beyond the method above, three samplers and a defensive mixture (the build's "next" rows;
+ * same arithmetic conventions as the default sampler):
+ *   0  i.i.d. draws, Horvitz-Thompson weight 1/pi_i with pi_i = 1 - (1 - q_i)^M (the method);
+ *   1  systematic draws, the stratified / systematic variants of [SANTA] ("Stochastic Sparse
+ *      Attention for Memory-Bound Inference", abstract) applied to team draws: one uniform
+ *      u (the Philox word of draw 0), the M points (r + u) / M, r = 0..M-1, on the CDF of q.
+ *      Team i's interval has length q_i and the points are 1/M apart, so it holds at least
+ *      one point with probability pi_i = min(1, M q_i); the weight is 1/pi_i;
+ *   2  i.i.d. draws with the Hansen-Hurwitz weight c_i / (M q_i), c_i the number of draws
+ *      of team i: the per-draw 1/p_i reweighting of [EXP] section 三 step 5.
+ * The defensive mixture of [EXP] section 八 (pitfall 4: mix a uniform share into the team
+ * distribution so that no weight explodes) samples from q_i = (1 - alpha) p_i + alpha / n;
+ * alpha = 0 is the plain method.
+ * Every sampler returns, per selected team, recip = 1 / weight, which the attention step
+ * uses exactly as it uses pi.
+ */
+#define ORACLE_SAMPLER_IID_HT 0
+#define ORACLE_SAMPLER_SYSTEMATIC 1
+#define ORACLE_SAMPLER_IID_HH 2
+
+/* q_i = (1 - alpha) p_i + alpha / n for i < n. */
+void oracle_mix(const double* p, int n, double alpha, double* q) {
+  for (int i = 0; i < n; ++i) q[i] = (1.0 - alpha) * p[i] + alpha / (double)n;
+}
+
+/* Systematic point r on the integer CDF: floor((r Z + t_u) / M) with t_u = floor(u Z) the
+ * draw-0 point.  Because r Z is an integer, this equals floor((r + u) Z / M) exactly, so
+ * t_r < C_i holds exactly when (r + u) / M * Z < C_i.  t_r < Z. */
+uint64_t oracle_systematic_point(uint64_t t_u, int r, int M, uint64_t Z) {
+  const unsigned __int128 num = (unsigned __int128)(uint64_t)r * Z + t_u;
+  return (uint64_t)(num / (unsigned __int128)(uint64_t)M);
+}
+
+/* M systematic draws from q[0..n) for unit (b, h); outputs as oracle_draw. */
+void oracle_draw_systematic(const double* q, int n, int M, uint64_t seed, int b, int h,
+                            int32_t* draws, uint64_t* t_out, uint64_t* cdf) {
+  if (n < 1 || n > ORACLE_MAX_TEAMS) return;
+  uint64_t* C = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)n);
+  if (!C) return;
+  uint64_t run = 0;
+  for (int i = 0; i < n; ++i) {
+    run += oracle_fixed_prob(q[i]);
+    C[i] = run;
+  }
+  const uint64_t Z = C[n - 1];
+  const uint64_t t_u = oracle_draw_point(seed, b, h, 0, Z);
+  for (int r = 0; r < M; ++r) {
+    const uint64_t t = oracle_systematic_point(t_u, r, M, Z);
+    draws[r] = oracle_cdf_search(C, n, t);
+    if (t_out) t_out[r] = t;
+  }
+  if (cdf)
+    for (int i = 0; i < n; ++i) cdf[i] = C[i];
+  free(C);
+}
+
+/* S = distinct drawn teams in ascending order, with recip = 1 / weight of each:
+ * sampler 0: 1 - (1 - q_i)^M; sampler 1: min(1, M q_i); sampler 2: M q_i / c_i.
+ * Returns |S|, or -1 for an unknown sampler. */
+int oracle_select_ex(const int32_t* draws, int M, const double* q, int n, int sampler,
+                     int32_t* sel, double* recip) {
+  if (sampler < ORACLE_SAMPLER_IID_HT || sampler > ORACLE_SAMPLER_IID_HH) return -1;
+  int count = 0;
+  for (int i = 0; i < n; ++i) {
+    int c = 0;
+    for (int r = 0; r < M; ++r)
+      if (draws[r] == i) ++c;
+    if (!c) continue;
+    sel[count] = i;
+    if (sampler == ORACLE_SAMPLER_IID_HT)
+      recip[count] = -expm1((double)M * log1p(-q[i]));
+    else if (sampler == ORACLE_SAMPLER_SYSTEMATIC)
+      recip[count] = fmin(1.0, (double)M * q[i]);
+    else
+      recip[count] = (double)M * q[i] / (double)c;
+    ++count;
+  }
+  return count;
+}
+
 /* ---------------------------------------------------------------- steps 4-5: attention */
 
 /* Raw score of token t of team i for query head hq: q . k / sqrt(d). */
@@ -400,5 +483,25 @@ int oracle_decode(const oracle_problem* pr, const double* reps, int M, uint64_t 
   oracle_draw(p, n, M, seed, b, h, draws, 0, 0);
   int count = oracle_select(draws, M, p, n, sel, pi);
   int err = oracle_attend(pr, b, h, sel, pi, count, out);
+  return err ? err : count;
+}
+
+/* oracle_decode with a sampler (0, 1, 2 as above) and a defensive mixture alpha in [0, 1]:
+ * q [max_teams] receives the sampling distribution, recip [M] the 1 / weight of each
+ * selected team.  Returns |S| or a negative error. */
+int oracle_decode_ex(const oracle_problem* pr, const double* reps, int M, uint64_t seed, int b,
+                     int h, int sampler, double alpha, int32_t* draws, int32_t* sel,
+                     double* recip, double* q, double* out) {
+  if (!(alpha >= 0.0 && alpha <= 1.0)) return -1;
+  int n = oracle_team_probs(pr, reps, b, h, 0, q);
+  if (n < 0) return n;
+  oracle_mix(q, n, alpha, q);
+  if (sampler == ORACLE_SAMPLER_SYSTEMATIC)
+    oracle_draw_systematic(q, n, M, seed, b, h, draws, 0, 0);
+  else
+    oracle_draw(q, n, M, seed, b, h, draws, 0, 0);
+  int count = oracle_select_ex(draws, M, q, n, sampler, sel, recip);
+  if (count < 0) return count;
+  int err = oracle_attend(pr, b, h, sel, recip, count, out);
   return err ? err : count;
 }
