@@ -148,7 +148,32 @@ typedef struct santa_decode_args {
   void* workspace;
   size_t workspace_bytes;
   int32_t* device_status;      /* one int32 the kernels OR SANTA_DEV_* bits into */
+  /* sampler variants (santa_sample / santa_decode; zero = the plain method) */
+  int32_t sampler;             /* santa_sampler */
+  float mix_alpha;             /* defensive mixture weight alpha in [0, 1] */
 } santa_decode_args;
+
+/*
+ * Samplers.  All draw from q_i = (1 - mix_alpha) p_i + mix_alpha / n, the team distribution
+ * with a uniform share mixed in: the defensive mixture of [EXP] section 八 (pitfall 4), which
+ * keeps every weight bounded.  mix_alpha = 0 is the plain distribution.  The output pi[k]
+ * always holds 1 / (weight of team sel_ids[k]), which santa_attend consumes as it is.
+ *   SANTA_SAMPLER_IID_HT      M i.i.d. draws; weight 1/pi_i, pi_i = 1 - (1 - q_i)^M
+ *                             (Horvitz-Thompson: the method of [ABS]).
+ *   SANTA_SAMPLER_SYSTEMATIC  one uniform u (the Philox word of draw 0), the M points
+ *                             (r + u) / M on the CDF; weight 1/pi_i with pi_i = min(1, M q_i)
+ *                             (the stratified / systematic variants of [SANTA], abstract).
+ *   SANTA_SAMPLER_IID_HH      M i.i.d. draws; weight c_i / (M q_i), c_i the draws of team i
+ *                             (Hansen-Hurwitz: the per-draw 1/p_i of [EXP] section 三 step 5).
+ * Non-default samplers and mix_alpha > 0 need every unit sampled inside one CTA's shared
+ * memory: max_teams <= 1024 and (G + 1) * ceil(max_teams / CL) <= 2048 for the plan's
+ * cluster size CL; other shapes return SANTA_ERR_UNSUPPORTED.
+ */
+typedef enum {
+  SANTA_SAMPLER_IID_HT = 0,
+  SANTA_SAMPLER_SYSTEMATIC = 1,
+  SANTA_SAMPLER_IID_HH = 2
+} santa_sampler;
 
 /*
  * Workspace.  A unit is served by one thread-block cluster (up to 16 CTAs sharing their
@@ -181,8 +206,9 @@ int santa_sample(const santa_decode_args* a, void* stream);
  * santa_attend — exact attention inside the teams listed in sel_ids[0..sel_count) of every
  * unit, each team weighted by 1/pi, combined as the Horvitz-Thompson ratio into out.
  * sel_ids / sel_count / pi may come from santa_sample or from the caller (distinct team
- * indices < n, any order, 0 < pi <= 1); entries out of range set SANTA_DEV_BAD_SEL and are
- * skipped.
+ * indices < n, any order, pi finite and > 0: the inclusion probability for Horvitz-Thompson
+ * weights, M q_i / c_i for Hansen-Hurwitz ones); entries out of range set SANTA_DEV_BAD_SEL
+ * and are skipped.
  * [ABS: "We compute exact attention scores within the sampled teams and reweight each
  * team's contribution by the inverse of its inclusion probability"; EXP steps 4-5.]
  */

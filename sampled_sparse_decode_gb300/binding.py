@@ -40,7 +40,13 @@ class _DecodeArgs(ctypes.Structure):
         ("sel_count", ctypes.c_void_p), ("pi", ctypes.c_void_p), ("team_probs", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("device_status", ctypes.c_void_p),
+        ("sampler", ctypes.c_int32), ("mix_alpha", ctypes.c_float),
     ]
+
+
+# Samplers (santa_sampler): i.i.d. draws with Horvitz-Thompson weights (the method),
+# systematic draws with Horvitz-Thompson weights, i.i.d. draws with Hansen-Hurwitz weights.
+SAMPLERS = {"iid_ht": 0, "systematic": 1, "iid_hh": 2}
 
 
 _lib = None
@@ -214,7 +220,7 @@ class DecodeBuffers:
 
 
 def _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed,
-          bufs: DecodeBuffers) -> _DecodeArgs:
+          bufs: DecodeBuffers, sampler: str = "iid_ht", mix_alpha: float = 0.0) -> _DecodeArgs:
     _req(q, "q", ndim=3)
     _req(k_pool, "k_pool", ndim=4)
     _req(v_pool, "v_pool", ndim=4)
@@ -239,6 +245,9 @@ def _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed,
     a.out, a.draw_ids, a.sel_ids = _ptr(bufs.out), _ptr(bufs.draw_ids), _ptr(bufs.sel_ids)
     a.sel_count, a.pi, a.team_probs = _ptr(bufs.sel_count), _ptr(bufs.pi), _ptr(bufs.team_probs)
     a.workspace, a.workspace_bytes = _ptr(bufs.workspace), bufs.workspace.numel()
+    if sampler not in SAMPLERS:
+        raise SantaError(f"unknown sampler {sampler!r} (one of {sorted(SAMPLERS)})")
+    a.sampler, a.mix_alpha = SAMPLERS[sampler], float(mix_alpha)
     a.device_status = _ptr(bufs.device_status)
     return a
 
@@ -254,10 +263,12 @@ def _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs=False, dense=Fa
 
 def santa_sample(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, seed: int,
                  bufs: DecodeBuffers | None = None, team_probs: bool = False,
-                 stream=None) -> DecodeBuffers:
-    """Team distribution, M draws, distinct set and inclusion probabilities."""
+                 stream=None, sampler: str = "iid_ht", mix_alpha: float = 0.0) -> DecodeBuffers:
+    """Team distribution, M draws, distinct set and 1 / weight per selected team (the
+    inclusion probability for the Horvitz-Thompson samplers)."""
     bufs = _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs)
-    a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs)
+    a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs, sampler,
+              mix_alpha)
     _check(lib().santa_sample(ctypes.byref(a), _stream(stream)), "santa_sample")
     return bufs
 
@@ -279,10 +290,12 @@ def santa_attend(q, k_pool, v_pool, page_table, seq_lens, sel_ids, sel_count, pi
 
 def santa_decode(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, seed: int,
                  bufs: DecodeBuffers | None = None, team_probs: bool = False,
-                 stream=None) -> DecodeBuffers:
-    """One SANTA++ decode step: sampling then Horvitz-Thompson attention."""
+                 stream=None, sampler: str = "iid_ht", mix_alpha: float = 0.0) -> DecodeBuffers:
+    """One SANTA++ decode step: sampling then weighted attention (Horvitz-Thompson by
+    default; see SAMPLERS and the defensive mixture weight mix_alpha)."""
     bufs = _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs)
-    a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs)
+    a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs, sampler,
+              mix_alpha)
     _check(lib().santa_decode(ctypes.byref(a), _stream(stream)), "santa_decode")
     return bufs
 

@@ -247,6 +247,32 @@ __device__ __forceinline__ V block_exclusive_scan(V v, V* warp_tot, V& total) {
   return pre + incl - v;
 }
 
+// Systematic draw point r: floor((r Z + t_u) / M), the fixed-point form of (r + u) Z / M
+// (t_u = floor(u Z), Z < 2^63, M <= 4096).  The 128-bit numerator is divided by two 64-bit
+// long-division steps; its high word is below M, so every partial numerator fits.
+// Kept out of line: the default sampler never calls it, and its long divisions would
+// otherwise lengthen the straight-line code every launch fetches.
+static __device__ __noinline__ unsigned long long systematic_point(unsigned long long t_u, int r,
+                                                                   int M, unsigned long long Z) {
+  const unsigned long long ru = static_cast<unsigned long long>(r);
+  const unsigned long long lo0 = ru * Z;
+  const unsigned long long lo = lo0 + t_u;
+  const unsigned long long hi = __umul64hi(ru, Z) + (lo < lo0 ? 1ull : 0ull);
+  const unsigned long long m = static_cast<unsigned long long>(M);
+  const unsigned long long x1 = (hi << 32) | (lo >> 32);
+  const unsigned long long q1 = x1 / m;
+  const unsigned long long x0 = ((x1 - q1 * m) << 32) | (lo & 0xffffffffull);
+  return (q1 << 32) | (x0 / m);
+}
+
+// 1 / weight of a selected team under the sampler: Horvitz-Thompson 1 - (1 - q)^M,
+// systematic min(1, M q), Hansen-Hurwitz M q / c (c draws of the team).
+__device__ __forceinline__ float team_recip(int sampler, float Mf, float q, int c) {
+  if (sampler == SANTA_SAMPLER_SYSTEMATIC) return fminf(1.f, Mf * q);
+  if (sampler == SANTA_SAMPLER_IID_HH) return Mf * q / static_cast<float>(c);
+  return -expm1f(Mf * log1pf(-q));
+}
+
 // Team of sampled slot k (0-based, k < the number of set bits): the k-th set bit of the
 // team mask, whose 32-bit words are grouped in 8 runs of `wpw` words with set-bit counts
 // gtot[0..7].  Slots follow ascending team order.
@@ -409,6 +435,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   const int* lpages = nullptr;            // local sampling: page id of every team of the unit
   const uint32_t* lmask = nullptr;        // local sampling: bit mask of the drawn teams
   const float* lps = nullptr;             // local sampling: team probabilities
+  const int* lcnt = nullptr;              // local sampling: draws per team
   int lwpw = 1;                           // local sampling: mask words per warp
   if (sampling) {
     const int cap = local ? (max(n, 1) + 3) / 4 * 4 : p.teams_per_cta;   // rows 16-byte aligned
@@ -511,6 +538,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       const bool out_writer = writer && rank == 0;
       unsigned long long run = 0ull, incl_t[kTpt];
       int rj = per > 0 ? jt / per : 0;                                // slice of team jt
+      const float alpha = p.mix_alpha;                                // defensive mixture
+      const float alpha_n = n > 0 ? alpha / static_cast<float>(n) : 0.f;
 #pragma unroll
       for (int u = 0; u < kTpt; ++u) {
         const int j = jt + u;
@@ -520,6 +549,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
           float pj = 0.f;
 #pragma unroll
           for (int g = 0; g < G; ++g) pj = fmaf(es[g * cap + j], s_pm[rj * G + g], pj);
+          if (alpha != 0.f) pj = fmaf(1.f - alpha, pj, alpha_n);       // q_j
           ps[j] = pj;
           flag[j] = 0;
           if (p.team_probs && out_writer) p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = pj;
@@ -547,19 +577,25 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       if (valid) {
         const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
                                      static_cast<uint32_t>(p.seed >> 32));
+        // systematic: every point derives from the uniform of draw 0
+        const bool systematic = p.sampler == SANTA_SAMPLER_SYSTEMATIC;
+        const bool count_draws = p.sampler == SANTA_SAMPLER_IID_HH;
         for (int r = tid; r < M; r += Tr::kThreads) {
-          const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(r), static_cast<uint32_t>(h),
+          const uint4 w = philox4x32_10(make_uint4(systematic ? 0u : static_cast<uint32_t>(r),
+                                                   static_cast<uint32_t>(h),
                                                    static_cast<uint32_t>(b), 0u),
                                         key);
           const unsigned long long a = 2ull * w.x + 1ull;            // u = a / 2^33
-          const unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
+          unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
+          if (systematic) t = systematic_point(t, r, M, Z);
           int lo_i = 0, hi_i = n - 1;
           while (lo_i < hi_i) {
             const int mid = (lo_i + hi_i) >> 1;
             if (t < cdf[mid]) hi_i = mid; else lo_i = mid + 1;
           }
           if (out_writer) p.draw_ids[static_cast<int64_t>(unit) * M + r] = lo_i;
-          flag[lo_i] = 1;
+          if (count_draws) atomicAdd(&flag[lo_i], 1);                 // draws per team
+          else flag[lo_i] = 1;
         }
       } else if (out_writer) {
         for (int r = tid; r < M; r += Tr::kThreads) p.draw_ids[static_cast<int64_t>(unit) * M + r] = -1;
@@ -573,13 +609,14 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         int cnt = 0;
         for (int w = warp * wpw; w < min(nw, (warp + 1) * wpw); ++w) {
           const int j = 32 * w + lane;
-          const uint32_t bits = __ballot_sync(0xffffffffu, valid && j < n && flag[j] == 1);
+          const uint32_t bits = __ballot_sync(0xffffffffu, valid && j < n && flag[j] > 0);
           if (lane == 0) mask[w] = bits;
           cnt += __popc(bits);
         }
         if (lane == 0) s_wi[warp] = cnt;
         lmask = mask;
         lps = ps;
+        lcnt = flag;
         lwpw = wpw;
       }
       __syncthreads();
@@ -788,7 +825,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       float piv = 0.f;
       if (k < total_sel) {
         team = select_team(lmask, s_wi, lwpw, k);
-        piv = -expm1f(Mf * log1pf(-lps[team]));
+        piv = team_recip(p.sampler, Mf, lps[team], lcnt[team]);
       }
       p.sel_ids[static_cast<int64_t>(unit) * M + k] = team;
       p.pi[static_cast<int64_t>(unit) * M + k] = piv;
@@ -805,7 +842,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       ListEntry e;
       if (local) {
         e.team = select_team(lmask, s_wi, lwpw, slot);
-        e.lw2 = -log2f(-expm1f(Mf * log1pf(-lps[e.team])));
+        e.lw2 = -log2f(team_recip(p.sampler, Mf, lps[e.team], lcnt[e.team]));
       } else {
         int owner = 0;
         while (owner + 1 < CL && s_base[owner + 1] <= slot) ++owner;
@@ -817,7 +854,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       const int64_t sidx = static_cast<int64_t>(unit) * M + slot;
       team = p.sel_ids[sidx];
       const float piv = p.pi[sidx];
-      ok = team >= 0 && team < n && piv > 0.f && piv <= 1.f;
+      ok = team >= 0 && team < n && piv > 0.f && isfinite(piv);   // pi = 1 / weight
       if (!ok) set_status(p.status, SANTA_DEV_BAD_SEL);
       lw2 = ok ? -log2f(piv) : 0.f;
     }

@@ -45,6 +45,8 @@ struct DecodeParams {
   int mode;                 // kMode*
   int teams_per_cta;        // sampling: ceil(max_teams / cluster size) <= kMaxTeamsPerCta
   int clusters_per_unit;    // NC
+  int sampler;              // SANTA_SAMPLER_*
+  float mix_alpha;          // q = (1 - alpha) p + alpha / n
   float* out;               // [B][Hq][d]
   int32_t* draw_ids;        // [B*Hkv][M]
   int32_t* sel_ids;         // [B*Hkv][M]  (read in attend mode)

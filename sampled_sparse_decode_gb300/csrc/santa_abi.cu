@@ -68,6 +68,9 @@ int check_inputs(const santa_decode_args* a) {
 
 int check_draws(const santa_decode_args* a) {
   if (a->num_draws < 1 || a->num_draws > kMaxDraws) return SANTA_ERR_UNSUPPORTED;
+  if (a->sampler < SANTA_SAMPLER_IID_HT || a->sampler > SANTA_SAMPLER_IID_HH)
+    return SANTA_ERR_INVALID_ARG;
+  if (!(a->mix_alpha >= 0.f && a->mix_alpha <= 1.f)) return SANTA_ERR_INVALID_ARG;
   if (!a->sel_ids || !a->sel_count || !a->pi) return SANTA_ERR_INVALID_ARG;
   if (!aligned(a->sel_ids, 4) || !aligned(a->sel_count, 4) || !aligned(a->pi, 4))
     return SANTA_ERR_INVALID_ARG;
@@ -305,6 +308,14 @@ int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
     return SANTA_ERR_INVALID_ARG;
   Plan pl;
   if ((rc = make_plan(a, mode, &pl))) return rc;
+  const bool variant = a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f;
+  if (sampling && variant) {
+    // the variants are implemented where a CTA samples its whole unit in shared memory
+    const int G = a->num_q_heads / a->num_kv_heads;
+    const int64_t per = ceil_div(a->max_teams, pl.cluster);
+    if (a->max_teams > santa::kMaxTeamsPerCta || (G + 1) * per > santa::kPubScores)
+      return SANTA_ERR_UNSUPPORTED;
+  }
   DecodeParams p = {};
   p.q = a->q;
   p.k_pool = a->k_pool;
@@ -326,6 +337,8 @@ int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   p.mode = mode;
   p.teams_per_cta = pl.tpc;
   p.clusters_per_unit = pl.clusters;
+  p.sampler = sampling ? a->sampler : SANTA_SAMPLER_IID_HT;
+  p.mix_alpha = sampling ? a->mix_alpha : 0.f;
   p.out = a->out;
   p.draw_ids = a->draw_ids;
   p.sel_ids = a->sel_ids;
@@ -389,7 +402,7 @@ const char* santa_status_string(int status) {
   switch (status) {
     case SANTA_OK: return "ok";
     case SANTA_ERR_INVALID_ARG: return "invalid argument (null, misaligned, bad size or short workspace)";
-    case SANTA_ERR_UNSUPPORTED: return "unsupported shape (dtype, head_dim, team_size, group, draws or teams)";
+    case SANTA_ERR_UNSUPPORTED: return "unsupported shape (dtype, head_dim, team_size, group, draws or teams), or a sampler variant for a shape sampled across CTAs";
     case SANTA_ERR_CUDA: return "CUDA runtime or launch error";
     case SANTA_ERR_DEVICE_STATUS: return "device status word reported an error";
     case SANTA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than santa_decode_noalloc's static buffer holds";

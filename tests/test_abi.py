@@ -57,7 +57,8 @@ def valid_args():
     ("num_q_heads", 36, UNSUPPORTED), ("num_q_heads", 30, INVALID), ("num_draws", 0, UNSUPPORTED),
     ("num_draws", 5000, UNSUPPORTED), ("max_teams", 20000, UNSUPPORTED), ("batch", 0, INVALID),
     ("num_pages", 0, INVALID), ("q", 0, INVALID), ("q", 0x10008, INVALID), ("sel_ids", 0, INVALID),
-    ("reps", 0, INVALID),
+    ("reps", 0, INVALID), ("sampler", 3, INVALID), ("sampler", -1, INVALID),
+    ("mix_alpha", -0.25, INVALID), ("mix_alpha", 1.5, INVALID), ("mix_alpha", float("nan"), INVALID),
 ])
 def test_sample_rejects_bad_arguments_on_host(lib, field, value, expect):
     a = valid_args()

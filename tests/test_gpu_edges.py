@@ -170,6 +170,18 @@ def test_bad_sampled_set_is_reported():
     torch.cuda.synchronize()
     assert bufs.status() & santa.DEV_BAD_SEL
     assert torch.isfinite(bufs.out).all()
+    # 1 / weight must be finite and positive (above 1 is fine: Hansen-Hurwitz weights)
+    for bad in (float("inf"), float("nan"), 0.0, -0.5):
+        sel = torch.tensor([[[0, 3, -1, -1]]], dtype=torch.int32, device="cuda")
+        pi = torch.tensor([[[1.7, bad, 0.0, 0.0]]], dtype=torch.float32, device="cuda")
+        bufs = santa.santa_attend(dw.q, dw.k_pool, dw.v_pool, dw.page_table, dw.seq_lens, sel,
+                                  cnt, pi)
+        torch.cuda.synchronize()
+        assert bufs.status() & santa.DEV_BAD_SEL, bad
+    pi = torch.tensor([[[1.7, 0.3, 0.0, 0.0]]], dtype=torch.float32, device="cuda")
+    bufs = santa.santa_attend(dw.q, dw.k_pool, dw.v_pool, dw.page_table, dw.seq_lens, sel, cnt, pi)
+    torch.cuda.synchronize()
+    assert bufs.status() == 0
 
 
 def test_update_reps_matches_build():
