@@ -56,9 +56,15 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
+    ap.add_argument("--mode", choices=["bench", "profile", "accuracy"], default="bench",
                     help="profile: W + K plain santa_decode (or --dense) steps on one copy of "
-                         "the inputs, for ncu captures")
+                         "the inputs, for ncu captures; accuracy: error of every sampler "
+                         "against dense attention over many seeds")
+    ap.add_argument("--sampler", choices=["iid_ht", "systematic", "iid_hh"], default="iid_ht",
+                    help="team sampler of the timed decode steps")
+    ap.add_argument("--mix-alpha", type=float, default=0.0,
+                    help="defensive mixture weight of the timed decode steps")
+    ap.add_argument("--seeds", type=int, default=256, help="accuracy mode: seeds per sampler")
     ap.add_argument("--dense", action="store_true", help="profile mode: the dense kernel")
     return ap.parse_args()
 
@@ -162,7 +168,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- oracle (CPU)
 
-def oracle_steps_per_s(wl, seconds, max_steps=None):
+def oracle_steps_per_s(wl, seconds, max_steps=None, sampler="iid_ht", alpha=0.0):
     """The fp64 oracle, single-threaded, timed per decode step (reps precomputed)."""
     import oracle
     pr = oracle.Problem(wl.q, wl.k_pool, wl.v_pool, wl.page_table, wl.seq_lens)
@@ -173,7 +179,7 @@ def oracle_steps_per_s(wl, seconds, max_steps=None):
     while True:
         for b in range(cfg.batch):
             for h in range(cfg.kv_heads):
-                oracle.decode(pr, reps, cfg.draws, steps, b, h)
+                oracle.decode_ex(pr, reps, cfg.draws, steps, b, h, sampler, alpha)
         steps += 1
         el = time.perf_counter() - t0
         if el >= seconds or (max_steps and steps >= max_steps):
@@ -195,7 +201,8 @@ def run_reference(args):
     reps = oracle.build_reps(pr, wl.page_fill)
     units = [(b, h) for b in range(cfg.batch) for h in range(cfg.kv_heads)]
     t0 = time.perf_counter()
-    oracle.decode(pr, reps, cfg.draws, 0, *units[0])
+    smp, alpha = args.sampler, args.mix_alpha
+    oracle.decode_ex(pr, reps, cfg.draws, 0, *units[0], smp, alpha)
     t_unit = time.perf_counter() - t0
     budget = 120.0
     per_step = budget / max(1, args.steps + args.warmup)
@@ -208,11 +215,11 @@ def run_reference(args):
     sample_units = units[:n_units]
     for s_ in range(args.warmup):
         for b, h in sample_units:
-            oracle.decode(pr, reps, cfg.draws, s_, b, h)
+            oracle.decode_ex(pr, reps, cfg.draws, s_, b, h, smp, alpha)
     t0 = time.perf_counter()
     for s_ in range(steps):
         for b, h in sample_units:
-            oracle.decode(pr, reps, cfg.draws, args.warmup + s_, b, h)
+            oracle.decode_ex(pr, reps, cfg.draws, args.warmup + s_, b, h, smp, alpha)
     el = (time.perf_counter() - t0) * len(units) / n_units
     v = steps / el
     sample = (f"{steps} steps, each decoding {n_units} of the {len(units)} (sequence, KV head) "
@@ -225,6 +232,7 @@ def run_reference(args):
         "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
                    "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "seq_len": cfg.seq_len,
                    "team_size": cfg.team_size, "draws": cfg.draws},
+        "sampler": {"name": smp, "mix_alpha": alpha},
         "cpu_baseline": {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -283,7 +291,8 @@ def run_ours(args):
                                      n_teams, M, dev)
     dbufs = Bn.DecodeBuffers.allocate(q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads, d, T,
                                       n_teams, M, dev, dense=True)
-    args_r = [Bn._args(q, ks[r], vs[r], reps[r], pt, lens, M, r, bufs) for r in range(R)]
+    args_r = [Bn._args(q, ks[r], vs[r], reps[r], pt, lens, M, r, bufs, args.sampler,
+                       args.mix_alpha) for r in range(R)]
     dargs_r = [Bn._args(q, ks[r], vs[r], None, pt, lens, 1, 0, dbufs) for r in range(R)]
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
@@ -377,6 +386,11 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     achieved = step_bytes / step_s / 1e9
 
+    # ---- accuracy proxy: relative L2 error of the estimate against dense attention, per
+    # query head, over 32 seeds (no model or dataset here: retention cannot be measured)
+    acc = accuracy_vs_dense(q, ks[0], vs[0], reps[0], pt, lens, M, args.sampler, args.mix_alpha,
+                            32, santa)
+
     # ---- end to end through the Python API, host buffers
     e2e = None
     if not args.no_e2e:
@@ -400,7 +414,8 @@ def run_ours(args):
                 dpt.copy_(hpt, non_blocking=True)
                 dlens.copy_(hlens, non_blocking=True)
                 santa.santa_decode(dq, ks[r], vs[r], reps[r], dpt, dlens, M, s, bufs=bufs,
-                                   stream=stream)
+                                   stream=stream, sampler=args.sampler,
+                                   mix_alpha=args.mix_alpha)
                 hout.copy_(bufs.out, non_blocking=True)
                 hsel.copy_(bufs.sel_ids, non_blocking=True)
                 hdraw.copy_(bufs.draw_ids, non_blocking=True)
@@ -425,7 +440,8 @@ def run_ours(args):
     # ---- CPU baseline (rank 0, single GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, n, el = oracle_steps_per_s(wl, args.cpu_seconds)
+        v, n, el = oracle_steps_per_s(wl, args.cpu_seconds, sampler=args.sampler,
+                                      alpha=args.mix_alpha)
         cpu = {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} whole decode steps ({units} units each) in {el:.1f} s, "
                          f"fp64 C oracle, one thread, reps precomputed"}
@@ -459,12 +475,63 @@ def run_ours(args):
                                "one launch per step",
                      "bytes_per_launch": step_bytes,
                      "traffic": recorded_traffic(cfg.name)},
+        "sampler": {"name": args.sampler, "mix_alpha": args.mix_alpha},
+        "accuracy": acc,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": steps_done,
         "clocks": clk,
     }
     print(json.dumps(line))
+
+
+def accuracy_vs_dense(q, k, v, reps, pt, lens, M, sampler, alpha, seeds, santa):
+    """Mean and 90th percentile over seeds and query heads of ||out - dense|| / ||dense||."""
+    import torch
+    dense = santa.santa_dense_decode(q, k, v, pt, lens).out.clone()
+    bufs = None
+    errs = []
+    for s_ in range(seeds):
+        bufs = santa.santa_decode(q, k, v, reps, pt, lens, M, 10_000 + s_, bufs=bufs,
+                                  sampler=sampler, mix_alpha=alpha)
+        e = (bufs.out - dense).norm(dim=-1) / dense.norm(dim=-1)
+        errs.append(e.flatten())
+    torch.cuda.synchronize()
+    assert bufs.status() == 0
+    e = torch.cat(errs).double()
+    return {"rel_l2_vs_dense_mean": float(e.mean()), "rel_l2_vs_dense_p90": float(e.quantile(0.9)),
+            "seeds": seeds, "metric": "||out - dense|| / ||dense|| per query head"}
+
+
+def run_accuracy(args):
+    """Every sampler (and a 5% defensive mixture) against dense attention on one workload."""
+    import numpy as np
+    import torch
+    import sampled_sparse_decode_gb300 as santa
+    from sampled_sparse_decode_gb300 import workloads as W
+    wl = W.generate(args.workload)
+    cfg = wl.cfg
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    q, k, v = t(wl.q), t(wl.k_pool), t(wl.v_pool)
+    pt, lens, fill = t(wl.page_table), t(wl.seq_lens), t(wl.page_fill)
+    reps = santa.santa_build_reps(k, fill)
+    rows = []
+    for sampler, alpha in [("iid_ht", 0.0), ("systematic", 0.0), ("iid_hh", 0.0),
+                           ("iid_ht", 0.05), ("systematic", 0.05)]:
+        a = accuracy_vs_dense(q, k, v, reps, pt, lens, cfg.draws, sampler, alpha, args.seeds,
+                              santa)
+        bufs = santa.santa_sample(q, k, v, reps, pt, lens, cfg.draws, 1, sampler=sampler,
+                                  mix_alpha=alpha)
+        torch.cuda.synchronize()
+        rows.append({"sampler": sampler, "mix_alpha": alpha, **a,
+                     "mean_sel": float(bufs.sel_count.double().mean())})
+    print(json.dumps({"mode": "accuracy", "workload": cfg.name, "draws": cfg.draws,
+                      "results": rows}))
 
 
 def run_profile(args):
@@ -503,6 +570,8 @@ def main():
     args = parse()
     if args.mode == "profile":
         run_profile(args)
+    elif args.mode == "accuracy":
+        run_accuracy(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
