@@ -118,6 +118,34 @@ int santa_update_reps(const void* k_pool, int dtype, int64_t num_pages, int num_
                       const int32_t* page_fill, float* reps, int32_t* device_status,
                       void* stream);
 
+/*
+ * santa_append_kv — one decode step's new token per (sequence, KV head), written into the
+ * paged cache, with the representative of its page brought up to date.  This is the step
+ * on either side of the decode path: tokens arrive one at a time and the teams they land in
+ * must stay described by their mean key.  [ABS: "the query scores one representative from
+ * each team"; EXP section 三 step 2, mean key; section 八 on keeping teams current as the
+ * sequence grows.]
+ *
+ *   k_new, v_new   [batch][num_kv_heads][head_dim], dtype (device).
+ *   seq_lens       [batch] current lengths L_b (device); the token goes to position L_b:
+ *                  slot L_b % team_size of page page_table[b][L_b / team_size].
+ *   k_pool, v_pool the paged cache, written at that slot.
+ *   reps           [num_pages][num_kv_heads][head_dim] fp32; the page's entry becomes the
+ *                  mean of its L_b % team_size + 1 valid keys, bit-identical to
+ *                  santa_build_reps / santa_update_reps on the grown cache (only that page's
+ *                  rows are read).
+ *   seq_lens_next  [batch] receives L_b + 1 (may be NULL; must not alias seq_lens).
+ *   device_status  SANTA_DEV_BAD_SEQLEN (L_b outside [0, max_teams * team_size)) or
+ *                  SANTA_DEV_BAD_PAGE; the sequence is then skipped.
+ * The page a token lands in must belong to that sequence alone (a shared-prefix page is
+ * never appended to).  Asynchronous on `stream`.
+ */
+int santa_append_kv(const void* k_new, const void* v_new, int dtype, int batch,
+                    int num_kv_heads, int team_size, int head_dim, int max_teams,
+                    int64_t num_pages, const int32_t* page_table, const int32_t* seq_lens,
+                    void* k_pool, void* v_pool, float* reps, int32_t* seq_lens_next,
+                    int32_t* device_status, void* stream);
+
 /* All inputs, outputs and scratch of one decode step (see the layouts above). */
 typedef struct santa_decode_args {
   /* inputs */

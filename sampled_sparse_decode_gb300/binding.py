@@ -69,6 +69,8 @@ def lib():
             "santa_decode_workspace_min_bytes": (sz, [i32] * 7),
             "santa_dense_workspace_bytes": (sz, [i32] * 7),
             "santa_sample": (i32, [A, vp]),
+            "santa_append_kv": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, vp, vp, vp,
+                                      vp, vp, vp, vp]),
             "santa_attend": (i32, [A, vp]),
             "santa_decode": (i32, [A, vp]),
             "santa_dense_decode": (i32, [A, vp]),
@@ -259,6 +261,33 @@ def _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs=False, dense=Fa
     _, Hkv, T, _ = k_pool.shape
     return DecodeBuffers.allocate(q.dtype, B, Hq, Hkv, d, T, page_table.shape[1], num_draws,
                                   q.device, team_probs=team_probs, dense=dense)
+
+
+def santa_append_kv(k_new, v_new, k_pool, v_pool, reps, page_table, seq_lens,
+                    seq_lens_next: torch.Tensor | None = None,
+                    device_status: torch.Tensor | None = None, stream=None):
+    """Write one new token per (sequence, KV head) (k_new, v_new [B][Hkv][d]) at position
+    seq_lens[b] of the paged cache and refresh its page's representative; seq_lens_next (if
+    given) receives seq_lens + 1.  All tensors on the device; nothing is allocated."""
+    _req(k_new, "k_new", ndim=3)
+    _req(v_new, "v_new", ndim=3)
+    _req(k_pool, "k_pool", ndim=4)
+    _req(reps, "reps", torch.float32, 3)
+    _req(page_table, "page_table", torch.int32, 2)
+    _req(seq_lens, "seq_lens", torch.int32, 1)
+    if seq_lens_next is not None:
+        _req(seq_lens_next, "seq_lens_next", torch.int32, 1)
+    if k_new.dtype not in _DTYPES or {k_new.dtype, v_new.dtype, k_pool.dtype, v_pool.dtype} != {k_new.dtype}:
+        raise SantaError("k_new, v_new, k_pool and v_pool must share one dtype")
+    P, Hkv, T, d = k_pool.shape
+    B = k_new.shape[0]
+    if tuple(k_new.shape) != (B, Hkv, d) or tuple(v_new.shape) != (B, Hkv, d) or \
+            tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise SantaError("k_new / v_new must be [B][Hkv][d] matching the pool")
+    _check(lib().santa_append_kv(_ptr(k_new), _ptr(v_new), _DTYPES[k_new.dtype], B, Hkv, T, d,
+                                 page_table.shape[1], P, _ptr(page_table), _ptr(seq_lens),
+                                 _ptr(k_pool), _ptr(v_pool), _ptr(reps), _ptr(seq_lens_next),
+                                 _ptr(device_status), _stream(stream)), "santa_append_kv")
 
 
 def santa_sample(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, seed: int,

@@ -24,6 +24,26 @@ struct RepsParams {
 };
 cudaError_t launch_reps(const RepsParams& p, int head_dim, cudaStream_t stream);
 
+// ---------------------------------------------------------------- token append
+struct AppendParams {
+  const void* k_new;        // [B][Hkv][d]
+  const void* v_new;        // [B][Hkv][d]
+  bool is_bf16;
+  int batch;
+  int num_kv_heads;
+  int team_size;
+  int max_teams;
+  int64_t num_pages;
+  const int32_t* page_table;  // [B][max_teams]
+  const int32_t* seq_lens;    // [B] current lengths: the new token goes to position L
+  void* k_pool;
+  void* v_pool;
+  float* reps;                // [P][Hkv][d]
+  int32_t* seq_lens_next;     // [B] L + 1, or nullptr
+  int32_t* status;
+};
+cudaError_t launch_append(const AppendParams& p, int head_dim, cudaStream_t stream);
+
 // ---------------------------------------------------------------- fused decode step
 constexpr int kModeDecode = 0;   // sample, then attend over the sampled teams
 constexpr int kModeSample = 1;   // sample only

@@ -426,6 +426,46 @@ int santa_update_reps(const void* k_pool, int dtype, int64_t num_pages, int num_
                  page_fill, reps, device_status, static_cast<cudaStream_t>(stream));
 }
 
+int santa_append_kv(const void* k_new, const void* v_new, int dtype, int batch,
+                    int num_kv_heads, int team_size, int head_dim, int max_teams,
+                    int64_t num_pages, const int32_t* page_table, const int32_t* seq_lens,
+                    void* k_pool, void* v_pool, float* reps, int32_t* seq_lens_next,
+                    int32_t* device_status, void* stream) {
+  if (dtype != SANTA_F32 && dtype != SANTA_BF16) return SANTA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return SANTA_ERR_UNSUPPORTED;
+  if (team_size != 64 && team_size != 128) return SANTA_ERR_UNSUPPORTED;
+  if (batch < 1 || num_kv_heads < 1 || max_teams < 1 || num_pages < 1)
+    return SANTA_ERR_INVALID_ARG;
+  if (max_teams > kMaxTeams) return SANTA_ERR_UNSUPPORTED;
+  if (!k_new || !v_new || !page_table || !seq_lens || !k_pool || !v_pool || !reps)
+    return SANTA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) ||
+      !aligned(v_pool, 16) || !aligned(reps, 16) || !aligned(page_table, 4) ||
+      !aligned(seq_lens, 4))
+    return SANTA_ERR_INVALID_ARG;
+  if ((seq_lens_next && !aligned(seq_lens_next, 4)) ||
+      (device_status && !aligned(device_status, 4)))
+    return SANTA_ERR_INVALID_ARG;
+  if (seq_lens_next == seq_lens) return SANTA_ERR_INVALID_ARG;   // read while written
+  santa::AppendParams p;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.is_bf16 = dtype == SANTA_BF16;
+  p.batch = batch;
+  p.num_kv_heads = num_kv_heads;
+  p.team_size = team_size;
+  p.max_teams = max_teams;
+  p.num_pages = num_pages;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.reps = reps;
+  p.seq_lens_next = seq_lens_next;
+  p.status = device_status;
+  return map_cuda(santa::launch_append(p, head_dim, static_cast<cudaStream_t>(stream)));
+}
+
 size_t santa_decode_workspace_bytes(int dtype, int batch, int num_q_heads, int num_kv_heads,
                                     int head_dim, int team_size, int max_teams, int num_draws) {
   return default_ws_bytes(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size,
