@@ -386,6 +386,22 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     achieved = step_bytes / step_s / 1e9
 
+    # ---- the step before the decode: one appended token per unit (santa_append_kv) at the
+    # last slot of every sequence, replayed from a CUDA graph of R calls
+    kn = torch.randn((cfg.batch, cfg.kv_heads, d), device=dev).to(q.dtype)
+    vn = torch.randn((cfg.batch, cfg.kv_heads, d), device=dev).to(q.dtype)
+    last = (lens - 1).contiguous()
+    nxt = torch.empty_like(lens)
+
+    def append_call(r):
+        santa.santa_append_kv(kn, vn, ks[r], vs[r], reps[r], pt, last, nxt, stream=stream)
+
+    def append_make(nsteps):
+        return capture(lambda: [append_call(r) for r in range(nsteps)])
+
+    sec_app, n_app, _ = timed(append_make, max(R, min(K, 1000)), W_)
+    append_us = sec_app / n_app * 1e6
+
     # ---- accuracy proxy: relative L2 error of the estimate against dense attention, per
     # query head, over 32 seeds (no model or dataset here: retention cannot be measured)
     acc = accuracy_vs_dense(q, ks[0], vs[0], reps[0], pt, lens, M, args.sampler, args.mix_alpha,
@@ -468,7 +484,8 @@ def run_ours(args):
                   "hbm_gbs": dense_kv / dense_s / 1e9},
         "speedup_vs_dense": dense_s / step_s,
         "kernels_us": {"decode": step_s * 1e6, "sample_only": smp_s * 1e6,
-                       "attend_only": att_s * 1e6, "dense": dense_s * 1e6},
+                       "attend_only": att_s * 1e6, "dense": dense_s * 1e6,
+                       "append_token": append_us},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "decode_kernel (fused sampling + split-K HT attention), "
