@@ -73,6 +73,11 @@ def lib():
             "oracle_dense": (i32, [P, i32, i32, vp]),
             "oracle_decode": (i32, [P, vp, i32, u64, i32, i32, vp, vp, vp, vp, vp]),
             "oracle_mix": (None, [vp, i32, dbl, vp]),
+            "oracle_vs_row_probs": (i32, [P, i32, i32, i32, vp]),
+            "oracle_vs_point": (u64, [u64, i32, i32, i32, i32, u64]),
+            "oracle_vs_draw": (i32, [P, i32, i32, i32, i32, u64, vp, vp, vp]),
+            "oracle_num_den_vs": (i32, [P, i32, i32, vp, vp, i32, i32, vp, vp, vp, vp]),
+            "oracle_attend_vs": (i32, [P, i32, i32, vp, vp, i32, i32, u64, vp, vp]),
             "oracle_systematic_point": (u64, [u64, i32, i32, u64]),
             "oracle_draw_systematic": (None, [vp, i32, i32, u64, i32, i32, vp, vp, vp]),
             "oracle_select_ex": (i32, [vp, i32, vp, i32, i32, vp, vp]),
@@ -303,3 +308,45 @@ def decode_ex(pr: Problem, reps: np.ndarray, M: int, seed: int, b: int, h: int,
                                         SAMPLERS[sampler], float(alpha), _ptr(draws), _ptr(sel),
                                         _ptr(rc), _ptr(q), _ptr(out)), "decode_ex")
     return UnitResult(draws, sel[:cnt].copy(), rc[:cnt].copy(), q[:pr.n_teams(b)].copy(), out)
+
+
+# ---------------------------------------------------------------- value-row sampling
+
+def vs_row_probs(pr: Problem, b: int, h: int, team: int) -> np.ndarray:
+    """Group-mean in-team distribution r over the team's valid tokens."""
+    r = np.zeros(pr.T, dtype=np.float64)
+    n = _check(lib().oracle_vs_row_probs(ctypes.byref(pr._c), b, h, team, _ptr(r)), "vs_row_probs")
+    return r[:n].copy()
+
+
+def vs_draw(pr: Problem, b: int, h: int, team: int, S: int, seed: int):
+    """Returns (idx [S] int32, t [S] uint64, C [len] uint64) for the row draws of a team."""
+    idx = np.zeros(S, dtype=np.int32)
+    t = np.zeros(S, dtype=np.uint64)
+    C = np.zeros(pr.T, dtype=np.uint64)
+    n = _check(lib().oracle_vs_draw(ctypes.byref(pr._c), b, h, team, S, seed, _ptr(idx), _ptr(t),
+                                    _ptr(C)), "vs_draw")
+    return idx, t, C[:n].copy()
+
+
+def num_den_vs(pr: Problem, b: int, h: int, sel, pi, S: int, idx, shift):
+    sel = np.ascontiguousarray(sel, dtype=np.int32)
+    pi = np.ascontiguousarray(pi, dtype=np.float64)
+    idx = np.ascontiguousarray(idx, dtype=np.int32).reshape(-1)
+    shift = np.ascontiguousarray(np.broadcast_to(np.asarray(shift, np.float64), (pr.G,)))
+    num = np.zeros((pr.G, pr.d), dtype=np.float64)
+    den = np.zeros(pr.G, dtype=np.float64)
+    _check(lib().oracle_num_den_vs(ctypes.byref(pr._c), b, h, _ptr(sel), _ptr(pi), sel.size, S,
+                                   _ptr(idx), _ptr(shift), _ptr(num), _ptr(den)), "num_den_vs")
+    return num, den
+
+
+def attend_vs(pr: Problem, b: int, h: int, sel, pi, S: int, seed: int):
+    """Returns (out [G][d], idx [|S|][S]) of the value-sampled estimate."""
+    sel = np.ascontiguousarray(sel, dtype=np.int32)
+    pi = np.ascontiguousarray(pi, dtype=np.float64)
+    idx = np.zeros((max(sel.size, 1), S), dtype=np.int32)
+    out = np.zeros((pr.G, pr.d), dtype=np.float64)
+    _check(lib().oracle_attend_vs(ctypes.byref(pr._c), b, h, _ptr(sel), _ptr(pi), sel.size, S,
+                                  seed, _ptr(idx), _ptr(out)), "attend_vs")
+    return out, idx[:sel.size].copy()

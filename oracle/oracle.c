@@ -436,6 +436,159 @@ int oracle_attend(const oracle_problem* pr, int b, int h, const int32_t* sel, co
   return 0;
 }
 
+/* ---------------------------------------------------------------- value-row sampling */
+
+/*
+ * Value-row sampling inside the selected teams ([SANTA] "Stochastic Sparse Attention for
+ * Memory-Bound Inference", abstract: draw value rows from the post-softmax distribution and
+ * gather-add them in place of the full P.V product).  With grouped-query attention one set
+ * of rows per team serves the G query heads: rows are drawn from the group-mean in-team
+ * distribution r_j = (1/G) sum_g exp(s_gj - m_gi) / Z_gi (m_gi, Z_gi the team's max and sum
+ * of exp for head g), and head g weighs a drawn row j by exp(s_gj - m_gi) / r_j.  That is an
+ * importance-sampling estimate of sum_j exp(s_gj - m_gi) v_j, unbiased given the team; the
+ * denominators Z_gi stay exact.  Row draw k of team i of unit (b, h) takes word 0 of
+ * Philox4x32-10 with counter (k, h, b, 1 + i) (team draws use word 3 = 0) and is decided
+ * exactly on the 62-bit fixed-point CDF of r, like the team draws.
+ */
+
+/* r_j for the valid tokens of team `team` of unit (b, h): r [len].  Returns len or < 0. */
+int oracle_vs_row_probs(const oracle_problem* pr, int b, int h, int team, double* r) {
+  const int n = num_teams(pr, b);
+  if (n < 0) return -1;
+  if (team < 0 || team >= n) return -3;
+  const int64_t page = team_page(pr, b, team);
+  if (page < 0 || page >= pr->num_pages) return -2;
+  const int len = team_len(pr, b, team);
+  const int G = pr->num_q_heads / pr->num_kv_heads;
+  for (int t = 0; t < len; ++t) r[t] = 0.0;
+  for (int g = 0; g < G; ++g) {
+    double m = -INFINITY, z = 0.0;
+    for (int t = 0; t < len; ++t) {
+      const double sc = token_score(pr, b, h * G + g, h, page, t);
+      if (sc > m) m = sc;
+    }
+    for (int t = 0; t < len; ++t) z += exp(token_score(pr, b, h * G + g, h, page, t) - m);
+    for (int t = 0; t < len; ++t)
+      r[t] += exp(token_score(pr, b, h * G + g, h, page, t) - m) / z / (double)G;
+  }
+  return len;
+}
+
+/* Position of row draw k of team `team` on an integer CDF of total Z (as oracle_draw_point,
+ * counter (k, h, b, 1 + team)). */
+uint64_t oracle_vs_point(uint64_t seed, int b, int h, int team, int k, uint64_t Z) {
+  uint32_t ctr[4] = {(uint32_t)k, (uint32_t)h, (uint32_t)b, (uint32_t)(1 + team)};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t w[4];
+  oracle_philox4x32_10(ctr, key, w);
+  unsigned __int128 prod = (unsigned __int128)(2ull * w[0] + 1ull) * Z;
+  return (uint64_t)(prod >> 33);
+}
+
+/* S row draws of team `team`: idx [S] token indices; t [S] and C [len] may be NULL.
+ * Returns len or < 0. */
+int oracle_vs_draw(const oracle_problem* pr, int b, int h, int team, int S, uint64_t seed,
+                   int32_t* idx, uint64_t* t_out, uint64_t* cdf) {
+  double r[1024];
+  if (pr->team_size > 1024) return -4;
+  const int len = oracle_vs_row_probs(pr, b, h, team, r);
+  if (len <= 0) return len < 0 ? len : -3;
+  uint64_t C[1024];
+  uint64_t run = 0;
+  for (int j = 0; j < len; ++j) {
+    run += oracle_fixed_prob(r[j]);
+    C[j] = run;
+  }
+  for (int k = 0; k < S; ++k) {
+    const uint64_t t = oracle_vs_point(seed, b, h, team, k, C[len - 1]);
+    idx[k] = oracle_cdf_search(C, len, t);
+    if (t_out) t_out[k] = t;
+  }
+  if (cdf)
+    for (int j = 0; j < len; ++j) cdf[j] = C[j];
+  return len;
+}
+
+/* Numerator and denominator with value-row sampling, given the row draws idx [count][S] and
+ * a caller-fixed shift m_g:
+ *   num_g = sum_c (1/pi_c) (1/S) sum_k exp(s_g,idx - m_g) / r_idx * v_idx   [G][d]
+ *   den_g = sum_c (1/pi_c) sum_{j in team} exp(s_gj - m_g)                  [G] (exact)
+ * Returns 0 or < 0. */
+int oracle_num_den_vs(const oracle_problem* pr, int b, int h, const int32_t* sel,
+                      const double* pi, int count, int S, const int32_t* idx,
+                      const double* shift, double* num, double* den) {
+  int err = check_sel(pr, b, sel, count);
+  if (err) return err;
+  const int d = pr->head_dim;
+  const int G = pr->num_q_heads / pr->num_kv_heads;
+  double r[1024];
+  if (pr->team_size > 1024) return -4;
+  for (int g = 0; g < G; ++g) {
+    den[g] = 0.0;
+    for (int k = 0; k < d; ++k) num[g * d + k] = 0.0;
+  }
+  for (int c = 0; c < count; ++c) {
+    const int64_t page = team_page(pr, b, sel[c]);
+    const int len = oracle_vs_row_probs(pr, b, h, sel[c], r);
+    if (len < 0) return len;
+    const double w = 1.0 / pi[c];
+    for (int g = 0; g < G; ++g) {
+      const int hq = h * G + g;
+      for (int t = 0; t < len; ++t) den[g] += w * exp(token_score(pr, b, hq, h, page, t) - shift[g]);
+      for (int k = 0; k < S; ++k) {
+        const int j = idx[c * S + k];
+        if (j < 0 || j >= len) return -5;
+        const double a = w * exp(token_score(pr, b, hq, h, page, j) - shift[g]) / r[j] / S;
+        for (int e = 0; e < d; ++e)
+          num[g * d + e] += a * elem(pr->v_pool, pr->dtype, kv_index(pr, page, h, j, e));
+      }
+    }
+  }
+  return 0;
+}
+
+/* The value-sampled estimate out_g = num_g / den_g (shift: the largest score among the
+ * sampled teams' tokens, as oracle_attend); idx [count][S] receives the row draws (may be
+ * NULL).  out [G][d].  Returns 0 or < 0. */
+int oracle_attend_vs(const oracle_problem* pr, int b, int h, const int32_t* sel,
+                     const double* pi, int count, int S, uint64_t seed, int32_t* idx_out,
+                     double* out) {
+  int err = check_sel(pr, b, sel, count);
+  if (err) return err;
+  if (count < 1 || S < 1) return -3;
+  const int d = pr->head_dim;
+  const int G = pr->num_q_heads / pr->num_kv_heads;
+  if (G > 8 || d > 128) return -4;
+  int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)count * (size_t)S);
+  if (!idx) return -6;
+  double shift[8], den[8], num[8 * 128];
+  for (int g = 0; g < G; ++g) {
+    double m = -INFINITY;
+    for (int c = 0; c < count; ++c) {
+      const int64_t page = team_page(pr, b, sel[c]);
+      const int len = team_len(pr, b, sel[c]);
+      for (int t = 0; t < len; ++t) {
+        const double s = token_score(pr, b, h * G + g, h, page, t);
+        if (s > m) m = s;
+      }
+    }
+    shift[g] = m;
+  }
+  for (int c = 0; c < count && !err; ++c) {
+    const int len = oracle_vs_draw(pr, b, h, sel[c], S, seed, idx + (size_t)c * S, 0, 0);
+    if (len < 0) err = len;
+  }
+  if (!err) err = oracle_num_den_vs(pr, b, h, sel, pi, count, S, idx, shift, num, den);
+  if (!err) {
+    for (int g = 0; g < G; ++g)
+      for (int k = 0; k < d; ++k) out[g * d + k] = num[g * d + k] / den[g];
+    if (idx_out)
+      for (size_t i = 0; i < (size_t)count * S; ++i) idx_out[i] = idx[i];
+  }
+  free(idx);
+  return err;
+}
+
 /* Dense softmax attention over every valid token of sequence b, for the G query heads of
  * KV head h: the quantity the estimator targets.  out [G][d]. */
 int oracle_dense(const oracle_problem* pr, int b, int h, double* out) {
