@@ -293,6 +293,28 @@ int santa_dense_decode(const santa_decode_args* a, void* stream);
  */
 int santa_decode_noalloc(const santa_decode_args* a, void* stream);
 
+/*
+ * santa_attend_vs — santa_attend with value-row sampling inside every listed team, in place
+ * of the full P.V product ([SANTA] "Stochastic Sparse Attention for Memory-Bound
+ * Inference", abstract: draw value rows from the post-softmax distribution and gather-add
+ * them).  The G query heads of a KV head share one set of S rows per team, drawn from the
+ * group-mean in-team softmax r_j; head g weighs a drawn row j by exp(s_gj - m_g) / r_j, and
+ * the team denominators stay exact, so the numerator is unbiased given the teams.  Row draw
+ * k of team i of unit (b, h) uses Philox4x32-10 word 0 of counter (k, h, b, 1 + i) with key
+ * `seed`, decided exactly on a 62-bit fixed-point CDF like the team draws.  Reads only the K
+ * rows of the listed teams and S value rows of each.
+ *   a          as for santa_attend (sel_ids, sel_count, pi in; out written), num_draws = M
+ *              (the slot dimension, <= 1024), seed = key of the row draws, workspace of at
+ *              least santa_attend_vs_workspace_bytes bytes (per-team partials).
+ *   value_rows S, rows drawn per team, 1..256.
+ *   value_ids  [B][Hkv][M][S] int32: the drawn rows (token index within the team), or NULL.
+ * Two launches on `stream`.
+ */
+size_t santa_attend_vs_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int num_draws);
+int santa_attend_vs(const santa_decode_args* a, int value_rows, int32_t* value_ids,
+                    void* stream);
+
 /* Size in bytes of the scratch array santa_decode_noalloc uses. */
 size_t santa_noalloc_scratch_bytes(void);
 

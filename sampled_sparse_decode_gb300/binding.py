@@ -69,6 +69,8 @@ def lib():
             "santa_decode_workspace_min_bytes": (sz, [i32] * 7),
             "santa_dense_workspace_bytes": (sz, [i32] * 7),
             "santa_sample": (i32, [A, vp]),
+            "santa_attend_vs": (i32, [A, i32, vp, vp]),
+            "santa_attend_vs_workspace_bytes": (sz, [i32] * 5),
             "santa_append_kv": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, vp, vp, vp,
                                       vp, vp, vp, vp]),
             "santa_attend": (i32, [A, vp]),
@@ -315,6 +317,33 @@ def santa_attend(q, k_pool, v_pool, page_table, seq_lens, sel_ids, sel_count, pi
     a.sel_ids, a.sel_count, a.pi = _ptr(sel_ids), _ptr(sel_count), _ptr(pi)
     _check(lib().santa_attend(ctypes.byref(a), _stream(stream)), "santa_attend")
     return bufs
+
+
+def santa_attend_vs(q, k_pool, v_pool, page_table, seq_lens, sel_ids, sel_count, pi,
+                    value_rows: int, seed: int, bufs: DecodeBuffers | None = None,
+                    value_ids: bool = False, stream=None):
+    """Attention over the given teams with value-row sampling inside each (value_rows rows
+    per team, drawn from the group-mean in-team softmax with key `seed`); writes bufs.out.
+    Returns (bufs, value_ids [B][Hkv][M][value_rows] int32 or None)."""
+    _req(sel_ids, "sel_ids", torch.int32, 3)
+    _req(sel_count, "sel_count", torch.int32, 2)
+    _req(pi, "pi", torch.float32, 3)
+    B, Hq, d = q.shape
+    Hkv = k_pool.shape[1]
+    M = sel_ids.shape[2]
+    bufs = _bufs_for(q, k_pool, page_table, M, bufs)
+    need = lib().santa_attend_vs_workspace_bytes(B, Hq, Hkv, d, M)
+    if need == 0:
+        raise SantaError("unsupported shape for santa_attend_vs")
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    vids = (torch.empty((B, Hkv, M, value_rows), dtype=torch.int32, device=q.device)
+            if value_ids else None)
+    a = _args(q, k_pool, v_pool, None, page_table, seq_lens, M, seed, bufs)
+    a.sel_ids, a.sel_count, a.pi = _ptr(sel_ids), _ptr(sel_count), _ptr(pi)
+    a.workspace, a.workspace_bytes = _ptr(ws), need
+    _check(lib().santa_attend_vs(ctypes.byref(a), value_rows, _ptr(vids), _stream(stream)),
+           "santa_attend_vs")
+    return bufs, vids
 
 
 def santa_decode(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, seed: int,

@@ -24,6 +24,37 @@ struct RepsParams {
 };
 cudaError_t launch_reps(const RepsParams& p, int head_dim, cudaStream_t stream);
 
+// ---------------------------------------------------------------- value-row sampling
+struct VsLaunch {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int32_t* sel_ids;
+  const int32_t* sel_count;
+  const float* pi;
+  bool bf16;
+  int batch;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int team_size;
+  int max_teams;
+  int num_draws;
+  int value_rows;
+  int64_t num_pages;
+  uint64_t seed;
+  float scale;
+  float* part_m;
+  float* part_z;
+  float* part_acc;
+  int32_t* value_ids;
+  float* out;
+  int32_t* status;
+};
+cudaError_t launch_value_sampled(const VsLaunch& l, cudaStream_t stream);
+
 // ---------------------------------------------------------------- token append
 struct AppendParams {
   const void* k_new;        // [B][Hkv][d]

@@ -426,6 +426,65 @@ int santa_update_reps(const void* k_pool, int dtype, int64_t num_pages, int num_
                  page_fill, reps, device_status, static_cast<cudaStream_t>(stream));
 }
 
+size_t santa_attend_vs_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int num_draws) {
+  if (check_shape(SANTA_F32, batch, num_q_heads, num_kv_heads, head_dim, 64, 1)) return 0;
+  if (num_draws < 1 || num_draws > 1024) return 0;
+  const size_t units = static_cast<size_t>(batch) * num_kv_heads;
+  const size_t G = static_cast<size_t>(num_q_heads / num_kv_heads);
+  const size_t ml = round_up(units * num_draws * G * sizeof(float), kAlign);
+  return kAlign + 2 * ml + units * num_draws * G * head_dim * sizeof(float);
+}
+
+int santa_attend_vs(const santa_decode_args* a, int value_rows, int32_t* value_ids,
+                    void* stream) {
+  int rc = check_inputs(a);
+  if (rc) return rc;
+  if (a->num_draws < 1 || a->num_draws > 1024 || value_rows < 1 || value_rows > 256)
+    return SANTA_ERR_UNSUPPORTED;
+  if (!a->sel_ids || !a->sel_count || !a->pi || !aligned(a->sel_ids, 4) ||
+      !aligned(a->sel_count, 4) || !aligned(a->pi, 4))
+    return SANTA_ERR_INVALID_ARG;
+  if (!a->out || !aligned(a->out, 16) || (value_ids && !aligned(value_ids, 4)))
+    return SANTA_ERR_INVALID_ARG;
+  const size_t need = santa_attend_vs_workspace_bytes(a->batch, a->num_q_heads, a->num_kv_heads,
+                                                      a->head_dim, a->num_draws);
+  if (!a->workspace || a->workspace_bytes < need) return SANTA_ERR_INVALID_ARG;
+  const size_t units = static_cast<size_t>(a->batch) * a->num_kv_heads;
+  const size_t G = static_cast<size_t>(a->num_q_heads / a->num_kv_heads);
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(a->workspace);
+  unsigned char* base = reinterpret_cast<unsigned char*>(round_up(raw, kAlign));
+  const size_t ml = round_up(units * a->num_draws * G * sizeof(float), kAlign);
+  santa::VsLaunch l;
+  l.q = a->q;
+  l.k_pool = a->k_pool;
+  l.v_pool = a->v_pool;
+  l.page_table = a->page_table;
+  l.seq_lens = a->seq_lens;
+  l.sel_ids = a->sel_ids;
+  l.sel_count = a->sel_count;
+  l.pi = a->pi;
+  l.bf16 = a->dtype == SANTA_BF16;
+  l.batch = a->batch;
+  l.num_q_heads = a->num_q_heads;
+  l.num_kv_heads = a->num_kv_heads;
+  l.head_dim = a->head_dim;
+  l.team_size = a->team_size;
+  l.max_teams = a->max_teams;
+  l.num_draws = a->num_draws;
+  l.value_rows = value_rows;
+  l.num_pages = a->num_pages;
+  l.seed = a->seed;
+  l.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(a->head_dim)));
+  l.part_m = reinterpret_cast<float*>(base);
+  l.part_z = reinterpret_cast<float*>(base + ml);
+  l.part_acc = reinterpret_cast<float*>(base + 2 * ml);
+  l.value_ids = value_ids;
+  l.out = a->out;
+  l.status = a->device_status;
+  return map_cuda(santa::launch_value_sampled(l, static_cast<cudaStream_t>(stream)));
+}
+
 int santa_append_kv(const void* k_new, const void* v_new, int dtype, int batch,
                     int num_kv_heads, int team_size, int head_dim, int max_teams,
                     int64_t num_pages, const int32_t* page_table, const int32_t* seq_lens,
