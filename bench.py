@@ -547,8 +547,55 @@ def run_accuracy(args):
         torch.cuda.synchronize()
         rows.append({"sampler": sampler, "mix_alpha": alpha, **a,
                      "mean_sel": float(bufs.sel_count.double().mean())})
+    # value-row sampling inside the teams, against the full P.V product on the same sets
+    sb = santa.santa_sample(q, k, v, reps, pt, lens, cfg.draws, 1)
+    dense = santa.santa_dense_decode(q, k, v, pt, lens).out.clone()
+
+    stream = torch.cuda.Stream()
+
+    def timed_us(fn, n=50, reps_=10):
+        """Mean device time per call: a CUDA graph of n calls, replayed reps_ times."""
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(n):
+                    fn()
+            g.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps_):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (n * reps_)
+
+    full = santa.santa_attend(q, k, v, pt, lens, sb.sel_ids, sb.sel_count, sb.pi)
+    vs_rows = [{"value_rows": 0, "name": "full P.V (santa_attend)",
+                "attend_us": timed_us(lambda: santa.santa_attend(q, k, v, pt, lens, sb.sel_ids,
+                                                                 sb.sel_count, sb.pi, bufs=full,
+                                                                 stream=stream)),
+                "rel_l2_vs_dense_mean": float(((full.out - dense).norm(dim=-1) /
+                                               dense.norm(dim=-1)).mean())}]
+    for S in (8, 16, 32, 64):
+        errs = []
+        for s_ in range(min(args.seeds, 64)):
+            vb, _ = santa.santa_attend_vs(q, k, v, pt, lens, sb.sel_ids, sb.sel_count, sb.pi, S,
+                                          20_000 + s_)
+            errs.append(((vb.out - dense).norm(dim=-1) / dense.norm(dim=-1)).flatten())
+        vb2 = vb
+        vs_rows.append({"value_rows": S, "name": "value-row sampling (santa_attend_vs)",
+                        "attend_us": timed_us(lambda: santa.santa_attend_vs(
+                            q, k, v, pt, lens, sb.sel_ids, sb.sel_count, sb.pi, S, 3,
+                            bufs=vb2, stream=stream)),
+                        "rel_l2_vs_dense_mean": float(torch.cat(errs).double().mean())})
     print(json.dumps({"mode": "accuracy", "workload": cfg.name, "draws": cfg.draws,
-                      "results": rows}))
+                      "results": rows, "value_sampling": vs_rows,
+                      "note": "attention only, on one sampled set per unit; CUDA graphs of 50 "
+                              "calls (inputs L2-resident: a comparison of the two, not a "
+                              "bandwidth figure)"}))
 
 
 def run_profile(args):
