@@ -47,6 +47,17 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 
 // Makes mbarrier initialisation visible to the asynchronous (bulk copy) proxy.
+// Programmatic dependent launch: the grid may be scheduled before the previous kernel in
+// its stream has finished; grid_dependency_wait() blocks until that kernel has completed and
+// its memory is visible (a no-op when the launch had no such dependency), and
+// grid_launch_dependents() lets the next kernel of the stream be scheduled early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Split cluster barrier; every thread of every CTA of the cluster executes each once, in
 // this order, with no other cluster barrier in between.  The arrive is relaxed: it orders no
 // memory operations, so it may only announce that remote reads whose values the thread has

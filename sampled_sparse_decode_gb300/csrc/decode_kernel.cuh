@@ -398,6 +398,11 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   __shared__ int s_base[17];
   __shared__ unsigned long long s_off, s_Z;
   __shared__ int s_abort, s_last;
+  // Launched with programmatic stream serialization: nothing of global memory is touched
+  // before the previous kernel of the stream has completed, and the next one may be
+  // scheduled (onto SMs this grid leaves free) from here on.
+  grid_dependency_wait();
+  grid_launch_dependents();
   if constexpr (BF16) {
     // The 128-byte-swizzled tile copies and the fragment addressing below both assume
     // 1 KiB-aligned stages; the layout is the same for every CTA, so all leave together.
@@ -1597,13 +1602,17 @@ cudaError_t decode_launch_t(const DecodeParams& p, dim3 grid, int cluster, cudaS
   cfg.blockDim = dim3(Tr::kThreads);
   cfg.dynamicSmemBytes = Tr::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel of the stream finishes (the kernel waits on it
+  // before touching global memory)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, decode_kernel<BF16, D, G, W>, p);
 }
 
