@@ -1079,15 +1079,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         part_m[tid] = mx;
         part_l[tid] = l;
       }
-      __syncthreads();
-      for (int i = tid; i < G * D; i += Tr::kThreads) {
-        const int g = i / D, k = i - g * D;
-        float a = 0.f;
-#pragma unroll
-        for (int w = 0; w < Tr::kWarps; ++w)
-          a = fmaf(arow[w * kMaxGroup + g], mrg_acc[(w * G + g) * D + k], a);
-        part[i] = a;
-      }
+      __syncthreads();      // the combine's push forms each partial quad from mrg_acc
     }
   } else if constexpr (BF16) {
     // ---- bf16 K/V: tensor-core scores and P.V (mma.sync m16n8k16, fp32 accumulate)
@@ -1258,16 +1250,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         part_m[tid] = mx;
         part_l[tid] = l;
       }
-      __syncthreads();
-      for (int i = tid; i < G * D; i += Tr::kThreads) {
-        const int g = i / D, k = i - g * D;
-        const int w0 = (k / (D / 2)) * 4;
-        float a = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w)
-          a = fmaf(arow[w * kMaxGroup + g], mrg_acc[((w0 + w) * G + g) * D + k], a);
-        part[i] = a;
-      }
+      __syncthreads();      // the combine's push forms each partial quad from mrg_acc
     }
   } else {
     // ---- fp32 K/V: CUDA-core scores and P.V
@@ -1426,12 +1409,32 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   const int qper = (kQuads + CL - 1) / CL;
   float4* comb_q = reinterpret_cast<float4*>(list);                 // [CL][qper] partial quads
   float* comb_ml = reinterpret_cast<float*>(comb_q + CL * qper);    // [CL][G][2] (m, l)
-  __syncthreads();                                                  // part complete
+  if constexpr (!BF16) __syncthreads();                             // part complete
   cluster_wait();                                                   // peers' reads are done
   if (attending) {
     for (int qi = tid; qi < kQuads; qi += Tr::kThreads) {
       const int r = qi / qper, k = qi - r * qper;
-      cluster.map_shared_rank(comb_q, r)[rank * qper + k] = reinterpret_cast<const float4*>(part)[qi];
+      float4 v;
+      if constexpr (BF16) {
+        // the CTA partial quad straight from the warp partials: weights arow[w][g] of
+        // every warp (wide) or of the four token tiles of this half of d
+        const int g = (4 * qi) / D, k0 = 4 * qi - g * D;
+        constexpr int kW = W ? Tr::kWarps : 4;
+        const int w0 = W ? 0 : (k0 / (D / 2)) * 4;
+        v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {
+          const float a = arow[w * kMaxGroup + g];
+          const float4 x = *reinterpret_cast<const float4*>(mrg_acc + ((w0 + w) * G + g) * D + k0);
+          v.x = fmaf(a, x.x, v.x);
+          v.y = fmaf(a, x.y, v.y);
+          v.z = fmaf(a, x.z, v.z);
+          v.w = fmaf(a, x.w, v.w);
+        }
+      } else {
+        v = reinterpret_cast<const float4*>(part)[qi];
+      }
+      cluster.map_shared_rank(comb_q, r)[rank * qper + k] = v;
     }
     if (tid < CL * G) {
       const int r = tid / G, g = tid - r * G;
