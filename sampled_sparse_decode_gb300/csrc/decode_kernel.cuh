@@ -1,42 +1,51 @@
 // decode_kernel.cuh — one SANTA++ decode step per (sequence, KV head) unit in one kernel:
 // representative scoring, GQA-mixed team softmax, Philox inverse-CDF sampling, the
-// deduplicated sampled set with its inclusion probabilities, exact attention inside the
-// sampled teams reweighted by 1/pi, and the Horvitz-Thompson combine.
+// deduplicated sampled set with its weights, exact attention inside the sampled teams
+// reweighted by 1/pi, and the Horvitz-Thompson combine.
 //
 // Method ("SANTA++: Sampling Attention through Representative Keys", abstract; explainer
 // "SANTA++：用代表性 Key 采样把 KV cache 读带宽砍掉 80%", section 三 steps 1-5, 3.1):
 //   s_{g,i} = q_g . rep_i / sqrt(d);  p_{g,i} = softmax_i(s_{g,.});  p_i = (1/G) sum_g p_{g,i}
 //   draw r: u = (word 0 of Philox4x32-10((r, h, b, 0), (lo32, hi32 of seed)) + 1/2) 2^-32,
-//           team = smallest i with u*Z < C_i  (C the fp64 running sum of p, Z = C_{n-1})
+//           team = smallest i with u*Z < C_i, decided exactly on the integer CDF of
+//           round(p_i 2^62) (floor(u Z) from a 128-bit product)
 //   S = distinct draws, pi_i = 1 - (1 - p_i)^M
 //   out_g = sum_{i in S} (1/pi_i) sum_{j in i} e^{s_j} v_j / sum_{i in S} (1/pi_i) sum_{j in i} e^{s_j}
+// (with the sampler variants of santa.h: systematic draws, Hansen-Hurwitz weights, and a
+// defensive uniform mixture of p).
 //
 // GB300 mapping.  A unit is served by NC thread-block clusters of CL CTAs (NC = 1 unless a
-// unit's work needs more CTAs than one cluster holds).  Inside a cluster:
-//   phase A  CTA r scores the representatives of teams [r*per, (r+1)*per) (one warp per team,
-//            coalesced 512-byte rows), publishes its per-head (max, sum) in shared memory;
-//            after a cluster barrier every CTA reads all peers' values with one parallel
-//            distributed-shared-memory (DSMEM) read and forms the same global softmax; the
-//            fp64 CDF slices' totals are exchanged the same way; each CTA resolves the draws
-//            whose u*Z falls in its slice by binary search, numbers its drawn teams and
-//            publishes them (team, -log2 pi) as a list; a third barrier exchanges the counts.
-//            Every reduction has a fixed order, so all CTAs (and all clusters of a unit)
-//            compute bit-identical sampled sets.
+// unit's work needs more CTAs than one cluster's tables hold).  Inside a cluster:
+//   phase A  CTA r scores the representatives of its slice of teams (page ids read first,
+//            rows staged with cp.async, 16 lanes per team), turns the slice into
+//            e = exp(s - m_slice) and pushes e, the page ids and (m_slice, z_slice) into
+//            every CTA of the cluster by distributed-shared-memory stores before one
+//            cluster barrier.  Every CTA then holds the whole unit: per-head global
+//            statistics (warp per head), p, the fixed-point CDF (one block scan), the M
+//            draws and a ballot bit mask of the drawn teams (slot k = k-th set bit).  All
+//            reductions run in a fixed order, so every CTA gets the same sampled set.
+//            Units with more teams than one CTA holds use a distributed variant (slices'
+//            totals and counts exchanged over three cluster barriers).
 //   phase B  the unit's sampled teams form a list of 64-token chunks; CTA g of the unit owns
-//            chunks [g*cps, (g+1)*cps), cps = ceil(chunks / CTAs) — balanced for any S; each
-//            chunk's team comes from its owner's list over DSMEM.
-//   phase C  thread 0 streams each chunk's K and V rows (contiguous in the paged pool) into
-//            a ring of shared-memory stages with two bulk copies (cp.async.bulk, the
-//            non-tensor TMA form) on an mbarrier; warp w scores tokens 8w..8w+7 with q in
-//            registers (16 lanes per token, 8-shuffle reduce-scatter to one head per lane),
-//            keeps a base-2 online softmax with -log2 pi folded into the scores, and
-//            accumulates P.V with lane l owning d/32 elements of every head.
-//   phase D  the 8 warps merge in shared memory; after a cluster barrier each CTA combines
-//            its slice of the outputs across the cluster's CTAs over DSMEM.  With NC > 1 the
+//            a contiguous range; each chunk's team, page and -log2 pi are resolved from the
+//            mask in shared memory; rank 0 of the first cluster writes the outputs of S.
+//   phase C  one thread streams each chunk's K and V into a ring of stages on mbarriers
+//            (bf16: 2-D tensor copies with 128-byte swizzle; fp32: bulk copies).  bf16 is
+//            consumed on tensor cores (mma.sync m16n8k16: scores S^T = K Q^T with the G
+//            heads as N, base-2 online softmax with -log2 pi folded in, P transposed by
+//            movmatrix and split bf16 hi + lo for O^T += V^T P^T); fp32 on CUDA cores.
+//            W = false: two CTAs per SM, warps split token tiles and halves of d.
+//            W = true (launches that fit one CTA per SM): six stages, two warp groups
+//            consuming alternate chunks on their own stages.
+//   phase D  the warps merge into a CTA partial; each CTA pushes the quads of the output
+//            slice rank r owns, with its (m, l), into rank r's shared memory; after one
+//            cluster barrier each CTA merges its slice in rank order.  With NC > 1 the
 //            cluster partials go to global scratch and the last CTA of the unit (an atomic
 //            ticket, no waiting) merges them in cluster order.
-// No wait is unbounded: mbarrier waits give up after 2 s (status bit, return through the
-// remaining barriers); every CTA executes every cluster barrier on every path.
+// The kernel is launched with programmatic stream serialization and touches global memory
+// only after griddepcontrol.wait.  No wait is unbounded: mbarrier waits give up after 2 s
+// (status bit, clean exit through the remaining barriers); every CTA executes every cluster
+// barrier on every path.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -87,8 +96,8 @@ struct DecodeTraits {
   static constexpr int kEplV = D / 32;
   static constexpr int kRing = kStages * kStageBytes;
   // phase A scratch inside the ring, for `cap` teams: cdf (uint64), es [8][cap], ps, flag,
-  // page ids and the drawn-team list (local path), then rows of representatives (fp32
-  // [rows][D]); rounded up to 128 bytes (the rows take 16-byte copies)
+  // page ids and room for the drawn-team bit mask (local path), then rows of
+  // representatives (fp32 [rows][D]); rounded up to 128 bytes (the rows take 16-byte copies)
   static constexpr size_t sample_scratch(int cap) {
     return ((sizeof(unsigned long long) + sizeof(float) * kMaxGroup + sizeof(float) +
              2 * sizeof(int) + sizeof(ListEntry)) * static_cast<size_t>(cap) + 127) / 128 * 128;
@@ -436,7 +445,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   // distributed path (softmax statistics, CDF totals and counts exchanged in three rounds).
   const int per = (n + CL - 1) / CL;
   const bool local = (G + 1) * per <= kPubScores && n <= kMaxTeamsPerCta;
-  ListEntry* llist = nullptr;             // local sampling: the drawn teams, in slot order
+  uint32_t* mask_area = nullptr;          // local sampling: room for the drawn-team mask
   const int* lpages = nullptr;            // local sampling: page id of every team of the unit
   const uint32_t* lmask = nullptr;        // local sampling: bit mask of the drawn teams
   const float* lps = nullptr;             // local sampling: team probabilities
@@ -449,7 +458,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     float* ps = es + kMaxGroup * cap;                                // [cap] team probability
     int* flag = reinterpret_cast<int*>(ps + cap);                    // [cap] drawn / slot
     int* pages = flag + cap;                                         // [cap] page ids (local)
-    llist = reinterpret_cast<ListEntry*>(pages + cap);               // [cap]
+    mask_area = reinterpret_cast<uint32_t*>(pages + cap);            // [cap] (nw words used)
     if (local) lpages = pages;
     float* rows = reinterpret_cast<float*>(smem + Tr::sample_scratch(cap));
     const int rows_cap = Tr::rep_rows(cap);
@@ -610,7 +619,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       // slots follow ascending team order): warp w ballots its run of wpw words
       {
         const int nw = (n + 31) / 32, wpw = (nw + 7) / 8;
-        uint32_t* mask = reinterpret_cast<uint32_t*>(llist);         // [nw]
+        uint32_t* mask = mask_area;                                  // [nw]
         int cnt = 0;
         for (int w = warp * wpw; w < min(nw, (warp + 1) * wpw); ++w) {
           const int j = 32 * w + lane;
