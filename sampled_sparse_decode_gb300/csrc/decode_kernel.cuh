@@ -369,6 +369,7 @@ __device__ __forceinline__ void score_teams(const DecodeParams& p, int b, int h,
     }
     __syncthreads();                               // rows may be refilled
   }
+  fence_proxy_async_smem();    // the staging rows may next be overwritten by bulk copies
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -436,6 +437,39 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   }
   __syncthreads();
 
+  // one chunk's K and V copies into its ring stage (or a bare arrival for an empty chunk)
+  const unsigned char* kpool = static_cast<const unsigned char*>(p.k_pool);
+  const unsigned char* vpool = static_cast<const unsigned char*>(p.v_pool);
+  auto issue_meta = [&](int ci, const ChunkMeta& m) {
+    const int stage = ci % S;
+    if (m.page >= 0) {
+      unsigned char* dst = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
+      mbar_arrive_expect_tx(&bar[stage], 2u * Tr::kChunkBytes);
+      if constexpr (BF16) {
+        // 64 rows x 64 elements (128 bytes, swizzled) per box; d = 128 takes two boxes
+        const int row = (m.page * p.num_kv_heads + h) * p.team_size + m.part * kChunk;
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx) {
+          tma_load_2d(dst + bx * kChunk * 128, &p.tmap_k, bx * 64, row, &bar[stage]);
+          tma_load_2d(dst + Tr::kChunkBytes + bx * kChunk * 128, &p.tmap_v, bx * 64, row,
+                      &bar[stage]);
+        }
+      } else {
+        const int64_t off = ((static_cast<int64_t>(m.page) * p.num_kv_heads + h) *
+                                 static_cast<int64_t>(p.team_size) + m.part * kChunk) *
+                            D * Tr::kEsize;
+        bulk_g2s(dst, kpool + off, Tr::kChunkBytes, &bar[stage]);
+        bulk_g2s(dst + Tr::kChunkBytes, vpool + off, Tr::kChunkBytes, &bar[stage]);
+      }
+    } else {
+      mbar_arrive(&bar[stage]);
+    }
+  };
+  // Decode steps sampled inside one CTA keep the phase-A scratch in the last stage(s) of the
+  // ring, so that this CTA's first `early_n` chunks can be copied as soon as S is known,
+  // while the chunk table is still being built from that scratch.
+  int early_n = 0;
+
   // ================================================================ phase A: sampling
   int total_sel = 0;                      // |S| of the unit
   // Exchange path: each CTA scores its slice of the teams and publishes the raw scores in
@@ -453,15 +487,21 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   int lwpw = 1;                           // local sampling: mask words per warp
   if (sampling) {
     const int cap = local ? (max(n, 1) + 3) / 4 * 4 : p.teams_per_cta;   // rows 16-byte aligned
-    unsigned long long* cdf = reinterpret_cast<unsigned long long*>(smem);   // [cap]
+    const size_t scr = Tr::sample_scratch(cap);
+    const int scr_stages = static_cast<int>((scr + Tr::kStageBytes - 1) / Tr::kStageBytes);
+    if (local && mode == kModeDecode && scr_stages < S) early_n = S - scr_stages;
+    unsigned char* scr_base = smem + static_cast<size_t>(early_n) * Tr::kStageBytes;
+    unsigned long long* cdf = reinterpret_cast<unsigned long long*>(scr_base);   // [cap]
     float* es = reinterpret_cast<float*>(cdf + cap);                 // [8][cap] scores, exps
     float* ps = es + kMaxGroup * cap;                                // [cap] team probability
     int* flag = reinterpret_cast<int*>(ps + cap);                    // [cap] drawn / slot
     int* pages = flag + cap;                                         // [cap] page ids (local)
     mask_area = reinterpret_cast<uint32_t*>(pages + cap);            // [cap] (nw words used)
     if (local) lpages = pages;
-    float* rows = reinterpret_cast<float*>(smem + Tr::sample_scratch(cap));
-    const int rows_cap = Tr::rep_rows(cap);
+    // staging rows for the representatives: the stages in front of the scratch, else the
+    // rest of the ring behind it
+    float* rows = reinterpret_cast<float*>(early_n > 0 ? smem : smem + scr);
+    const int rows_cap = early_n > 0 ? early_n * Tr::kStageBytes / (D * 4) : Tr::rep_rows(cap);
     float* pub_scores = reinterpret_cast<float*>(list);              // [G][per], published
     int* pub_pages = reinterpret_cast<int*>(pub_scores + G * per);   // [per], published
     int lo = min(rank * per, n);
@@ -638,6 +678,24 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
 #pragma unroll
       for (int w = 0; w < 8; ++w) count += s_wi[w];
       total_sel = count;
+      if (early_n > 0 && tid < early_n) {
+        // this CTA's first chunks (the chunk range as phase B computes it), one per thread,
+        // into the stages in front of the scratch; phase B fills the same table entries
+        const int ctas = CL * NC, gidx = cidx * CL + rank;
+        const int tot = count * cpt, per_cta = (tot + ctas - 1) / ctas;
+        const int cb = min(gidx * per_cta, tot), nch = min(tot - cb, per_cta);
+        const int ci = tid;
+        if (ci < nch) {
+          const int c = cb + ci, slot = c / cpt, part = c - slot * cpt;
+          const int team = select_team(lmask, s_wi, lwpw, slot);
+          const int page = pages[team];
+          const bool pok = page >= 0 && page < p.num_pages;
+          const int vt = pok ? max(0, min(min(p.team_size, L - team * p.team_size) - part * kChunk,
+                                          kChunk))
+                             : 0;
+          issue_meta(ci, ChunkMeta{vt > 0 ? page : -1, vt, 0.f, part});
+        }
+      }
     } else {
       score_teams<D, G>(p, b, h, lo, nl, qs, rows, rows_cap, es, cap, flag);
       // per-head (max, sum of exp) over the scored teams
@@ -892,35 +950,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   cluster_arrive_relaxed();
 
   // ================================================================ phase C: stream + compute
-  const unsigned char* kpool = static_cast<const unsigned char*>(p.k_pool);
-  const unsigned char* vpool = static_cast<const unsigned char*>(p.v_pool);
-  auto issue = [&](int ci) {
-    const int stage = ci % S;
-    const ChunkMeta m = table[ci];
-    if (m.page >= 0) {
-      unsigned char* dst = smem + static_cast<size_t>(stage) * Tr::kStageBytes;
-      mbar_arrive_expect_tx(&bar[stage], 2u * Tr::kChunkBytes);
-      if constexpr (BF16) {
-        // 64 rows x 64 elements (128 bytes, swizzled) per box; d = 128 takes two boxes
-        const int row = (m.page * p.num_kv_heads + h) * p.team_size + m.part * kChunk;
-#pragma unroll
-        for (int bx = 0; bx < D / 64; ++bx) {
-          tma_load_2d(dst + bx * kChunk * 128, &p.tmap_k, bx * 64, row, &bar[stage]);
-          tma_load_2d(dst + Tr::kChunkBytes + bx * kChunk * 128, &p.tmap_v, bx * 64, row,
-                      &bar[stage]);
-        }
-      } else {
-        const int64_t off = ((static_cast<int64_t>(m.page) * p.num_kv_heads + h) *
-                                 static_cast<int64_t>(p.team_size) + m.part * kChunk) *
-                            D * Tr::kEsize;
-        bulk_g2s(dst, kpool + off, Tr::kChunkBytes, &bar[stage]);
-        bulk_g2s(dst + Tr::kChunkBytes, vpool + off, Tr::kChunkBytes, &bar[stage]);
-      }
-    } else {
-      mbar_arrive(&bar[stage]);
-    }
-  };
-  if (tid < min(S, n_chunks)) issue(tid);
+  auto issue = [&](int ci) { issue_meta(ci, table[ci]); };
+  if (tid >= early_n && tid < min(S, n_chunks)) issue(tid);   // chunks < early_n are out
 
   float* mrg_acc = reinterpret_cast<float*>(smem);                   // [8][G][D]
   float* mrg_m = mrg_acc + Tr::kWarps * G * D;                       // [8][8]
