@@ -257,3 +257,37 @@ def test_full_size_sampled_units(name):
     for b in range(cfg.batch):
         for h in range(cfg.kv_heads):
             assert (pi[b, h, :cnt[b, h]] > 0).all() and (pi[b, h, :cnt[b, h]] <= 1).all()
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 6, 8])
+@pytest.mark.parametrize("head_dim,batch", [(128, 2), (64, 1), (128, 40)])
+def test_every_group_size(G, head_dim, batch):
+    """Every instantiated group size, both head sizes; batch 40 takes the two-CTA-per-SM
+    variant, the others the wide one.  Draws, S and pi as in the sampling parity test; the
+    whole step compared with the oracle where the sampled sets agree."""
+    wl = make(dict(cfg="qwen7b_32k_b1_m31", batch=batch, q_heads=2 * G, kv_heads=2,
+                   head_dim=head_dim, seq_len=1100 if batch > 2 else 2600, draws=24))
+    cfg = wl.cfg
+    dw = DeviceWorkload(wl)
+    pr = problem(wl)
+    reps_o = oracle.build_reps(pr, wl.page_fill)
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    want_wide = batch <= 2
+    plan = santa.santa_decode_plan(dw.q, dw.k_pool, dw.page_table, cfg.draws, "decode")
+    assert plan["wide"] == want_wide, plan
+    bufs = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
+                              cfg.draws, 31, team_probs=True)
+    torch.cuda.synchronize()
+    assert bufs.status() == 0
+    tol = TOL_OUT[cfg.dtype]
+    checked = 0
+    for b in range(0, cfg.batch, max(1, cfg.batch // 4)):
+        for h in range(cfg.kv_heads):
+            check_unit_sampling(wl, pr, reps_o, bufs, cfg.draws, 31, b, h)
+            r = oracle.decode(pr, reps_o, cfg.draws, 31, b, h)
+            cnt = int(bufs.sel_count[b, h])
+            if cnt == r.sel.size and np.array_equal(bufs.sel_ids[b, h, :cnt].cpu().numpy(), r.sel):
+                got = bufs.out[b, h * G:(h + 1) * G].cpu().numpy()
+                assert np.abs(got - r.out).max() <= tol
+                checked += 1
+    assert checked >= 1
