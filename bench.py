@@ -78,6 +78,18 @@ def dist_setup(n_gpus):
     return world, rank, local
 
 
+def job_rate(seconds, steps, world, device):
+    """Whole-job rate of `world` replicas that each ran `steps` steps: the slowest rank's time
+    (max over ranks, any torch.distributed backend) and world * steps / that time.
+    Returns (rate, slowest seconds)."""
+    import torch
+    if world > 1:
+        t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        seconds = float(t.item())
+    return world * steps / seconds, seconds
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -348,12 +360,8 @@ def run_ours(args):
 
     # ---- headline: whole decode steps
     sec, steps_done, (c0, c1) = timed(rounds(lib.santa_decode, args_r), K, W_)
-    if world > 1:
-        tt = torch.tensor([sec], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        sec = float(tt.item())
+    value, sec = job_rate(sec, steps_done, world, dev)
     step_s = sec / steps_done
-    value = world * steps_done / sec
 
     # realised |S| of the R seeds (the graph replays them)
     sel_total = 0
@@ -446,11 +454,8 @@ def run_ours(args):
         for s in range(K_e):
             e2e_step(W_ + s)
         el = time.perf_counter() - t0
-        if world > 1:
-            tt = torch.tensor([el], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            el = float(tt.item())
-        e2e = {"value": world * K_e / el, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+        e2e_rate, el = job_rate(el, K_e, world, dev)
+        e2e = {"value": e2e_rate, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": K_e}
 
     # ---- CPU baseline (rank 0, single GPU only)
