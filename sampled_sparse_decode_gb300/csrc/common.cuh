@@ -144,6 +144,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       : "memory");
 }
 
+// Bring a tensor-map descriptor (kernel parameter) into the descriptor cache ahead of its
+// first use by a tensor copy.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // ---------------------------------------------------------------- warp matrix fragments
 
 // Four 8x8 b16 matrices from shared memory (row addresses given per lane).

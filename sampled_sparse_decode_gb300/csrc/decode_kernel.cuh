@@ -411,6 +411,12 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   // Launched with programmatic stream serialization: nothing of global memory is touched
   // before the previous kernel of the stream has completed, and the next one may be
   // scheduled (onto SMs this grid leaves free) from here on.
+  if constexpr (BF16) {
+    if (attending && tid == 0) {       // descriptors are launch constants: no wait needed
+      prefetch_tensormap(&p.tmap_k);
+      prefetch_tensormap(&p.tmap_v);
+    }
+  }
   grid_dependency_wait();
   grid_launch_dependents();
   if constexpr (BF16) {
