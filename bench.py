@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--mix-alpha", type=float, default=0.0,
                     help="defensive mixture weight of the timed decode steps")
     ap.add_argument("--seeds", type=int, default=256, help="accuracy mode: seeds per sampler")
+    ap.add_argument("--draws", type=int, default=None,
+                    help="override the workload's number of draws M (for M sweeps)")
     ap.add_argument("--dense", action="store_true", help="profile mode: the dense kernel")
     return ap.parse_args()
 
@@ -207,7 +209,7 @@ def run_reference(args):
         return
     import oracle
     from sampled_sparse_decode_gb300 import workloads as W
-    wl = W.generate(args.workload)
+    wl = W.generate(args.workload, **({'draws': args.draws} if args.draws else {}))
     cfg = wl.cfg
     pr = oracle.Problem(wl.q, wl.k_pool, wl.v_pool, wl.page_table, wl.seq_lens)
     reps = oracle.build_reps(pr, wl.page_fill)
@@ -272,7 +274,7 @@ def run_ours(args):
         if world > 1:
             torch.distributed.barrier()
 
-    wl = W.generate(args.workload)
+    wl = W.generate(args.workload, **({'draws': args.draws} if args.draws else {}))
     cfg = wl.cfg
     lib = Bn.lib()
     esize = 2 if cfg.dtype == "bf16" else 4
@@ -531,7 +533,7 @@ def run_accuracy(args):
     import torch
     import sampled_sparse_decode_gb300 as santa
     from sampled_sparse_decode_gb300 import workloads as W
-    wl = W.generate(args.workload)
+    wl = W.generate(args.workload, **({'draws': args.draws} if args.draws else {}))
     cfg = wl.cfg
 
     def t(a):
@@ -609,7 +611,7 @@ def run_profile(args):
     import torch
     import sampled_sparse_decode_gb300 as santa
     from sampled_sparse_decode_gb300 import workloads as W
-    wl = W.generate(args.workload)
+    wl = W.generate(args.workload, **({'draws': args.draws} if args.draws else {}))
     cfg = wl.cfg
 
     def t(a):
