@@ -72,6 +72,10 @@ __global__ void __launch_bounds__(kVsThreads) vs_team_kernel(const VsParams p) {
   const int M = p.num_draws, S = p.value_rows, T = p.team_size;
   const int64_t unit = static_cast<int64_t>(b) * p.num_kv_heads + h;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, lane16 = lane & 15;
+  // launched with programmatic serialisation: wait for the kernel that wrote the sampled set,
+  // then let the combine kernel be scheduled (it waits for this grid to finish)
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int count = p.sel_count[unit];
   if (slot >= count || slot >= M) return;
   float* pm = p.part_m + (unit * M + slot) * G;
@@ -209,12 +213,27 @@ __global__ void __launch_bounds__(kVsThreads) vs_team_kernel(const VsParams p) {
 #pragma unroll
   for (int g = 0; g < G; ++g) acc[g] = 0.f;
   const unsigned char* vsrc = static_cast<const unsigned char*>(p.v_pool) + base * D * Ly::kEsize;
-  for (int k = half; k < S; k += kParts) {
-    const int j = idx[k];
-    const float v = BF16 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(vsrc)[j * D + e])
-                         : reinterpret_cast<const float*>(vsrc)[j * D + e];
+  // rows in batches of 8: all loads of a batch are in flight before any is used
+  for (int k0 = half; k0 < S; k0 += 8 * kParts) {
+    float v[8];
 #pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = fmaf(wgt[g * kMaxValueRows + k], v, acc[g]);
+    for (int u = 0; u < 8; ++u) {
+      const int k = k0 + u * kParts;
+      v[u] = 0.f;
+      if (k < S) {
+        const int j = idx[k];
+        v[u] = BF16 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(vsrc)[j * D + e])
+                    : reinterpret_cast<const float*>(vsrc)[j * D + e];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = k0 + u * kParts;
+      if (k < S) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[g] = fmaf(wgt[g * kMaxValueRows + k], v[u], acc[g]);
+      }
+    }
   }
   float* red = reinterpret_cast<float*>(smem + Ly::kK);         // K rows are no longer needed
   __syncthreads();
@@ -236,16 +255,23 @@ __global__ void __launch_bounds__(kVsThreads) vs_team_kernel(const VsParams p) {
 }
 
 // out_g = sum_c (1/pi_c) e^(m_c - mx) acc_c / sum_c (1/pi_c) e^(m_c - mx) Z_c over the unit's
-// slots c in order.  Warp g forms head g's slot weights (lanes over slots) into shared
-// memory [G][M]; then every thread sums its output elements over the slots.
+// slots c.  Warp g forms head g's slot weights (lanes over slots) into shared memory [G][M].
+// Then four groups of threads each sum every fourth slot of every output quad, with the
+// loads of 8 slots in flight at once, and the four group sums are added in fixed order.
+constexpr int kCombThreads = 1024;
+constexpr int kCombGroups = 4;
+
 template <int D, int G>
-__global__ void __launch_bounds__(kVsThreads) vs_combine_kernel(const VsParams p) {
+__global__ void __launch_bounds__(kCombThreads) vs_combine_kernel(const VsParams p) {
+  constexpr int kQuads = G * D / 4;
   extern __shared__ float s_w[];                       // [G][M]
   __shared__ float s_den[kMaxGroup];
+  __shared__ float4 s_red[kCombGroups][kQuads];
   const int h = blockIdx.x, b = blockIdx.y;
   const int M = p.num_draws;
   const int64_t unit = static_cast<int64_t>(b) * p.num_kv_heads + h;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dependency_wait();                              // the team kernel's partials
   const int count = max(0, min(p.sel_count[unit], M));
   if (warp < G) {
     float mx = -INFINITY;
@@ -262,14 +288,45 @@ __global__ void __launch_bounds__(kVsThreads) vs_combine_kernel(const VsParams p
     if (lane == 0) s_den[warp] = den;
   }
   __syncthreads();
-  float* out = p.out + (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D;
-  for (int i = tid; i < G * D; i += kVsThreads) {
-    const int g = i / D;
-    float num = 0.f;
-    for (int c = 0; c < count; ++c)
-      num = fmaf(s_w[g * M + c], p.part_acc[(unit * M + c) * G * D + i], num);
+  const float4* acc = reinterpret_cast<const float4*>(p.part_acc) + unit * M * kQuads;
+  for (int item = tid; item < kCombGroups * kQuads; item += kCombThreads) {
+    const int grp = item / kQuads, qi = item - grp * kQuads;
+    const int g = (4 * qi) / D;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = grp; c0 < count; c0 += 8 * kCombGroups) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * kCombGroups;
+        v[u] = c < count ? acc[static_cast<int64_t>(c) * kQuads + qi] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u * kCombGroups;
+        const float w = c < count ? s_w[g * M + c] : 0.f;
+        a.x = fmaf(w, v[u].x, a.x);
+        a.y = fmaf(w, v[u].y, a.y);
+        a.z = fmaf(w, v[u].z, a.z);
+        a.w = fmaf(w, v[u].w, a.w);
+      }
+    }
+    s_red[grp][qi] = a;
+  }
+  __syncthreads();
+  float4* out = reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D);
+  for (int qi = tid; qi < kQuads; qi += kCombThreads) {
+    const int g = (4 * qi) / D;
+    float4 sum = s_red[0][qi];
+#pragma unroll
+    for (int grp = 1; grp < kCombGroups; ++grp) {
+      sum.x += s_red[grp][qi].x;
+      sum.y += s_red[grp][qi].y;
+      sum.z += s_red[grp][qi].z;
+      sum.w += s_red[grp][qi].w;
+    }
     const float den = s_den[g];
-    out[i] = den > 0.f ? num / den : 0.f;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    out[qi] = make_float4(sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv);
   }
 }
 
@@ -281,16 +338,28 @@ cudaError_t vs_launch_t(const VsParams& p, int batch, cudaStream_t stream) {
   // the attribute once per device, for the largest team size and slot count
   cudaError_t e = ensure_dynamic_smem(vs_team_kernel<BF16, D, G>, Ly::kBytes(128), flag);
   if (e != cudaSuccess) return e;
-  vs_team_kernel<BF16, D, G><<<dim3(p.num_draws, p.num_kv_heads, batch), kVsThreads, smem,
-                               stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // both kernels may be scheduled while the previous kernel of the stream finishes; each
+  // waits on it before reading what it wrote
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_draws, p.num_kv_heads, batch);
+  cfg.blockDim = dim3(kVsThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, vs_team_kernel<BF16, D, G>, p)) != cudaSuccess) return e;
   const size_t csmem = sizeof(float) * G * static_cast<size_t>(p.num_draws);
   static std::atomic<unsigned long long> cflag{0};
   if ((e = ensure_dynamic_smem(vs_combine_kernel<D, G>, sizeof(float) * G * kMaxVsSlots,
                                cflag)) != cudaSuccess)
     return e;
-  vs_combine_kernel<D, G><<<dim3(p.num_kv_heads, batch), kVsThreads, csmem, stream>>>(p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(p.num_kv_heads, batch);
+  cfg.blockDim = dim3(kCombThreads);
+  cfg.dynamicSmemBytes = csmem;
+  return cudaLaunchKernelEx(&cfg, vs_combine_kernel<D, G>, p);
 }
 
 }  // namespace
