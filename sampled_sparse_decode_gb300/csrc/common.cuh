@@ -46,7 +46,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                : "memory");
 }
 
-// Makes mbarrier initialisation visible to the asynchronous (bulk copy) proxy.
 // Programmatic dependent launch: the grid may be scheduled before the previous kernel in
 // its stream has finished; grid_dependency_wait() blocks until that kernel has completed and
 // its memory is visible (a no-op when the launch had no such dependency), and
@@ -85,6 +84,7 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Makes mbarrier initialisation visible to the asynchronous (bulk copy) proxy.
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
