@@ -56,10 +56,11 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["bench", "profile", "accuracy"], default="bench",
+    ap.add_argument("--mode", choices=["bench", "profile", "accuracy", "loop"], default="bench",
                     help="profile: W + K plain santa_decode (or --dense) steps on one copy of "
                          "the inputs, for ncu captures; accuracy: error of every sampler "
-                         "against dense attention over many seeds")
+                         "against dense attention over many seeds; loop: a generation of "
+                         "--gen-tokens steps (append + decode), fresh vs held sampled sets")
     ap.add_argument("--sampler", choices=["iid_ht", "systematic", "iid_hh"], default="iid_ht",
                     help="team sampler of the timed decode steps")
     ap.add_argument("--mix-alpha", type=float, default=0.0,
@@ -68,6 +69,10 @@ def parse():
     ap.add_argument("--draws", type=int, default=None,
                     help="override the workload's number of draws M (for M sweeps)")
     ap.add_argument("--dense", action="store_true", help="profile mode: the dense kernel")
+    ap.add_argument("--gen-tokens", type=int, default=4096,
+                    help="loop mode: tokens generated after the workload's context")
+    ap.add_argument("--refresh", default="16,64,256",
+                    help="loop mode: hold periods R of the sampled set (comma separated)")
     return ap.parse_args()
 
 
@@ -605,6 +610,135 @@ def run_accuracy(args):
                               "bandwidth figure)"}))
 
 
+def _mean_ci(xs):
+    """Mean and half-width of its 95% confidence interval (normal approximation)."""
+    n = len(xs)
+    m = sum(xs) / n
+    sd = statistics.stdev(xs) if n > 1 else 0.0
+    return m, 1.96 * sd / math.sqrt(n)
+
+
+def run_loop(args):
+    """A generation at the workload's context (the explainer's pitfall 2: sampling variance
+    over autoregressive steps).  Every step appends the next token's K/V (santa_append_kv)
+    and decodes with that step's query.  The policies are:
+      dense       santa_dense_decode every step (also the reference of the errors);
+      fresh       santa_decode every step (a new sampled set per step);
+      held R      santa_decode every R steps, santa_attend over the held set in between.
+    Per policy: step latency (append + decode; mean and 95% CI over the steps), the relative
+    L2 error of each step's output against dense, and the error of the outputs summed over
+    the first t steps (how the per-step errors add up over a generation)."""
+    import dataclasses
+    import numpy as np
+    import torch
+    import sampled_sparse_decode_gb300 as santa
+    from sampled_sparse_decode_gb300 import workloads as W
+    cfg = W.CONFIGS[args.workload]
+    if args.draws:
+        cfg = dataclasses.replace(cfg, draws=args.draws)
+    steps, L0, T = args.gen_tokens, cfg.seq_len, cfg.team_size
+    B, Hkv, Hq, d = cfg.batch, cfg.kv_heads, cfg.q_heads, cfg.head_dim
+    wl = W.generate(cfg, seq_lens=[L0 + steps] * B)
+    # the generated tokens are the continuation of each sequence; their slots start as NaN
+    pos = L0 + np.arange(steps)
+    kn = np.empty((steps, B, Hkv, d), dtype=wl.k_pool.dtype)
+    vn = np.empty_like(kn)
+    nan_bits = np.array([0x7FC0], np.uint16)[0] if wl.k_pool.dtype == np.uint16 else np.nan
+    for b in range(B):
+        pages, slots = wl.page_table[b, pos // T], pos % T
+        kn[:, b] = wl.k_pool[pages, :, slots]
+        vn[:, b] = wl.v_pool[pages, :, slots]
+        wl.k_pool[pages, :, slots] = nan_bits
+        wl.v_pool[pages, :, slots] = nan_bits
+    fill0 = np.zeros(wl.k_pool.shape[0], np.int32)
+    for b in range(B):
+        for i in range(-(-L0 // T)):
+            fill0[wl.page_table[b, i]] = min(T, L0 - i * T)
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+                torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    k0, v0 = t(wl.k_pool), t(wl.v_pool)
+    kp, vp = torch.empty_like(k0), torch.empty_like(v0)
+    pt, fill = t(wl.page_table), t(fill0)
+    knd, vnd, qs = t(kn), t(vn), t(W.loop_queries(cfg, steps))
+    lens0 = torch.full((B,), L0, dtype=torch.int32, device="cuda")
+    reps = torch.empty((wl.k_pool.shape[0], Hkv, d), dtype=torch.float32, device="cuda")
+    flush = torch.empty(2 * torch.cuda.get_device_properties(0).L2_cache_size,
+                        dtype=torch.uint8, device="cuda")
+    dense_out = torch.empty((steps, B, Hq, d), dtype=torch.float32, device="cuda")
+    periods = [int(r) for r in args.refresh.split(",") if r]
+    policies = [("dense", None), ("fresh", 1)] + [(f"held {r}", r) for r in periods]
+    results = []
+    for name, R in policies:
+        kp.copy_(k0)
+        vp.copy_(v0)
+        santa.santa_build_reps(kp, fill, reps=reps)
+        lens = [lens0.clone(), torch.empty_like(lens0)]
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        outs = torch.empty_like(dense_out)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        dec = att = None
+        for s in range(steps):
+            flush.zero_()                          # L2 holds nothing of this layer
+            torch.cuda._sleep(1_000_000)           # the device runs behind the host
+            ev[s][0].record()
+            santa.santa_append_kv(knd[s], vnd[s], kp, vp, reps, pt, lens[s % 2],
+                                  lens[(s + 1) % 2], status)
+            cur = lens[(s + 1) % 2]
+            if R is None:
+                dec = santa.santa_dense_decode(qs[s], kp, vp, pt, cur, bufs=dec)
+                res = dec
+            elif s % R == 0:
+                dec = santa.santa_decode(qs[s], kp, vp, reps, pt, cur, cfg.draws, s, bufs=dec)
+                res = dec
+            else:
+                att = santa.santa_attend(qs[s], kp, vp, pt, cur, dec.sel_ids, dec.sel_count,
+                                         dec.pi, bufs=att)
+                res = att
+            ev[s][1].record()
+            outs[s].copy_(res.out)
+        torch.cuda.synchronize()
+        st = int(status.item()) | dec.status() | (att.status() if att is not None else 0)
+        if st:
+            raise SystemExit(f"{name}: device status {st}")
+        if R is None:
+            dense_out.copy_(outs)
+        us = [a.elapsed_time(b) * 1e3 for a, b in ev]
+        m, ci = _mean_ci(us)
+        row = {"policy": name, "refresh": R, "step_us_mean": m, "step_us_ci95": ci,
+               "step_us_p50": statistics.median(us)}
+        if R is not None:
+            diff = (outs - dense_out).double()
+            ref = dense_out.double()
+            per_step = (diff.norm(dim=-1) / ref.norm(dim=-1)).mean(dim=(1, 2))
+            acc = (diff.cumsum(0).norm(dim=-1) / ref.cumsum(0).norm(dim=-1)).mean(dim=(1, 2))
+            row["rel_l2_step_mean"] = float(per_step.mean())
+            row["rel_l2_step_p90"] = float(per_step.quantile(0.9))
+            row["rel_l2_accumulated"] = {str(n): float(acc[n - 1]) for n in
+                                         (1, 16, 64, 256, 1024, steps) if n <= steps}
+        results.append(row)
+    dm, dci = results[0]["step_us_mean"], results[0]["step_us_ci95"]
+    for row in results[1:]:
+        m, ci = row["step_us_mean"], row["step_us_ci95"]
+        r = dm / m
+        row["speedup_vs_dense"] = r
+        row["speedup_ci95"] = r * math.sqrt((dci / dm) ** 2 + (ci / m) ** 2)
+    print(json.dumps({
+        "mode": "loop", "workload": cfg.name, "context_start": L0, "generated": steps,
+        "draws": cfg.draws, "results": results,
+        "l2": "flushed before every step (a write of 2x the L2 size)",
+        "timing": "CUDA events around each step's append + decode; a spin kernel before "
+                  "every step keeps the device behind the host, so no launch gap is timed",
+        "queries": "per step: each head's mixture part fixed, fresh 0.3 * N(0, I) noise",
+        "error": "||out - dense|| / ||dense|| per query head, mean over heads; accumulated: "
+                 "the same for the outputs summed over the first t steps"}))
+
+
 def run_profile(args):
     """A short run for ncu: one copy of the inputs, W + K steps launched on the stream."""
     import numpy as np
@@ -643,6 +777,8 @@ def main():
         run_profile(args)
     elif args.mode == "accuracy":
         run_accuracy(args)
+    elif args.mode == "loop":
+        run_loop(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

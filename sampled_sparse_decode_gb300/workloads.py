@@ -108,6 +108,18 @@ def _unit_rng(seed: int, b: int, h: int, salt: int = 0) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, b, h, salt])))
 
 
+def _mixture_queries(rng: np.random.Generator, mus: np.ndarray, G: int, d: int):
+    """Each query head takes 3 distinct components of its KV head's mixture:
+    q_g = 0.7 * mean of their means + 0.3 * N(0, I).  Returns (q, the 0.7 * mean part)."""
+    q = np.empty((G, d))
+    base = np.empty((G, d))
+    for g in range(G):
+        comps = rng.choice(64, size=3, replace=False)
+        base[g] = 0.7 * mus[comps].mean(axis=0)
+        q[g] = base[g] + 0.3 * rng.standard_normal(d)
+    return q, base
+
+
 def _gen_unit(cfg: Config, b: int, h: int, n_tok: int):
     """q [G][d], K [n_tok][d], V [n_tok][d] in float64 for unit (b, h)."""
     rng = _unit_rng(cfg.data_seed, b, h)
@@ -117,10 +129,7 @@ def _gen_unit(cfg: Config, b: int, h: int, n_tok: int):
         K = rng.standard_normal((n_tok, d))
     elif cfg.keys == "mixture":
         mus = rng.standard_normal((64, d))
-        q = np.empty((G, d))
-        for g in range(G):
-            comps = rng.choice(64, size=3, replace=False)
-            q[g] = 0.7 * mus[comps].mean(axis=0) + 0.3 * rng.standard_normal(d)
+        q, _ = _mixture_queries(rng, mus, G, d)
         comp = np.empty(n_tok, dtype=np.int64)
         pos = 0
         while pos < n_tok:
@@ -207,3 +216,28 @@ def generate(cfg: Config | str, seq_lens=None, invalid_fill: float = 0.0,
         for i in range(-(-L // T)):
             page_fill[page_table[b, i]] = min(T, L - i * T)
     return Workload(cfg, q, k_pool, v_pool, page_table, lens, page_fill)
+
+
+def loop_queries(cfg: Config | str, steps: int) -> np.ndarray:
+    """Queries of a generation of `steps` tokens, [steps][B][Hq][d] in the workload's dtype.
+
+    Each query head keeps the mixture components its step-0 query was built from and draws
+    fresh noise every step: q_t = 0.7 * mean of the components + 0.3 * N(0, I) (for Gaussian
+    keys, q_t ~ N(0, I)).  The noise of step t comes from its own seeded stream, so the
+    sequence does not depend on how many steps are generated."""
+    if isinstance(cfg, str):
+        cfg = CONFIGS[cfg]
+    G, d = cfg.group, cfg.head_dim
+    out = np.empty((steps, cfg.batch, cfg.q_heads, d), dtype=np.float64)
+    for b in range(cfg.batch):
+        for h in range(cfg.kv_heads):
+            if cfg.keys == "mixture":
+                rng = _unit_rng(cfg.data_seed, b, h)
+                _, base = _mixture_queries(rng, rng.standard_normal((64, d)), G, d)
+                scale = 0.3
+            else:
+                base, scale = np.zeros((G, d)), 1.0
+            for t in range(steps):
+                noise = _unit_rng(cfg.data_seed, b, h, salt=1 + t).standard_normal((G, d))
+                out[t, b, h * G:(h + 1) * G] = base + scale * noise
+    return _store(out, cfg.dtype)

@@ -6,6 +6,8 @@
   the parity tolerance of the oracle's means.
 - A decode loop (append, decode, repeat) keeps matching the oracle on identical sampled sets
   as the sequences grow across page boundaries.
+- A sampled set held over later steps (one refresh, then attention only) matches the
+  oracle's attention over the same held set on the grown cache.
 """
 import numpy as np
 import pytest
@@ -128,6 +130,51 @@ def test_decode_loop_matches_oracle_as_sequences_grow():
                         assert np.abs(got - r.out).max() <= TOL_OUT["bf16"]
     torch.cuda.synchronize()
     assert (lens[24 % 2].cpu().numpy() == np.array(lens0) + 24).all()
+
+
+def test_held_set_across_appends_matches_oracle():
+    """A sampled set held over later steps (sampled once, then santa_attend with each step's
+    own query on the grown cache): the outputs match the oracle's attention over the same
+    held set and inclusion probabilities.  Sequences 1 and 2 open a new team during the
+    hold, which the held set does not contain."""
+    lens0 = [1000, 250, 127]
+    wl, dw = _grown("qwen7b_32k_b8_m64", lens0, seq_len=1536)
+    cfg = wl.cfg
+    M, G = cfg.draws, cfg.group
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    held = santa.santa_sample(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
+                              M, 3)
+    lens = [dw.seq_lens.clone(), torch.empty_like(dw.seq_lens)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_rng = np.random.default_rng(6)
+    checked = 0
+    for s in range(24):
+        k_new, v_new = _new_tokens(wl, 2000 + s)
+        santa.santa_append_kv(to_torch(k_new), to_torch(v_new), dw.k_pool, dw.v_pool, reps,
+                              dw.page_table, lens[s % 2], lens[(s + 1) % 2], status)
+        cur = lens[(s + 1) % 2]
+        q = W.f32_to_bf16_bits(q_rng.standard_normal(wl.q.shape).astype(np.float32))
+        bufs = santa.santa_attend(to_torch(q), dw.k_pool, dw.v_pool, dw.page_table, cur,
+                                  held.sel_ids, held.sel_count, held.pi)
+        if s in (4, 23):
+            torch.cuda.synchronize()
+            assert bufs.status() == 0 and held.status() == 0 and int(status.item()) == 0
+            L = cur.cpu().numpy()
+            pr = oracle.Problem(q, _host(dw.k_pool), _host(dw.v_pool), wl.page_table, L)
+            for b in range(cfg.batch):
+                for h in range(cfg.kv_heads):
+                    cnt = int(held.sel_count[b, h])
+                    sel = held.sel_ids[b, h, :cnt].cpu().numpy()
+                    pi = held.pi[b, h, :cnt].cpu().numpy().astype(np.float64)
+                    assert sel.max() < -(-lens0[b] // cfg.team_size)
+                    want = oracle.attend(pr, b, h, sel, pi)
+                    got = bufs.out[b, h * G:(h + 1) * G].cpu().numpy()
+                    assert np.abs(got - want).max() <= TOL_OUT["bf16"]
+                    checked += 1
+    assert checked == 2 * cfg.batch * cfg.kv_heads
+    final = lens[24 % 2].cpu().numpy()
+    T = cfg.team_size
+    assert -(-final[1] // T) > -(-lens0[1] // T) and -(-final[2] // T) > -(-lens0[2] // T)
 
 
 def test_append_reports_full_sequences_and_bad_pages():
