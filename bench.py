@@ -15,9 +15,10 @@ value      steps/s of whole decode steps with inputs resident in HBM, K steps re
 roofline   the fused decode kernel (one launch per step): algorithmic bytes per launch (the
            team representatives, K and V of the sampled teams, q, out) / its mean duration
            (CUDA events over graph-replayed launches), against the measured HBM copy bandwidth.
-e2e        the same steps through the Python API with pinned host buffers: per step the
-           query, page table and lengths go host->device and out, draw/sampled ids, pi and
-           |S| come back device->host, then the stream is synchronised.
+e2e        the same steps through the Python API with pinned host buffers: per step one
+           copy takes the query, page table and lengths host->device (StepInputs), a
+           PreparedDecode runs the step, one copy brings out, draw/sampled ids, pi and |S|
+           back device->host (packed DecodeBuffers), then the stream is synchronised.
 dense      the in-run dense split-K decode kernel on the same buffers (speed reference).
 cpu_baseline  the fp64 C oracle, single-threaded, on a bounded sample of steps.
 --impl reference  times that oracle alone (the reference arm of this benchmark).
@@ -417,41 +418,46 @@ def run_ours(args):
     sec_app, n_app, _ = timed(append_make, max(R, min(K, 1000)), W_)
     append_us = sec_app / n_app * 1e6
 
+    # ---- the representatives of the whole cache (santa_build_reps, once after prefill): a
+    # rebuild of every rotation copy in place from its own keys (the same values again)
+    def reps_make(nsteps):
+        return capture(lambda: [santa.santa_build_reps(ks[r], fill, reps=reps[r], stream=stream)
+                                for r in range(nsteps)])
+
+    sec_rep, n_rep, _ = timed(reps_make, max(R, min(K, 200)), W_)
+    reps_us = sec_rep / n_rep * 1e6
+    valid_tokens = int(wl.page_fill.astype(np.int64).sum())
+    reps_bytes = valid_tokens * cfg.kv_heads * d * esize + reps0.numel() * 4
+
     # ---- accuracy proxy: relative L2 error of the estimate against dense attention, per
     # query head, over 32 seeds (no model or dataset here: retention cannot be measured)
     acc = accuracy_vs_dense(q, ks[0], vs[0], reps[0], pt, lens, M, args.sampler, args.mix_alpha,
                             32, santa)
 
-    # ---- end to end through the Python API, host buffers
+    # ---- end to end through the Python API, host buffers: per step one host->device copy
+    # of the step's inputs (StepInputs), the decode (PreparedDecode over the rotation's
+    # buffers), one device->host copy of the five outputs (packed DecodeBuffers) and a
+    # stream synchronisation
     e2e = None
     if not args.no_e2e:
-        pin = dict(pin_memory=True)
-        hq = q.cpu().clone().pin_memory()
-        hpt, hlens = pt.cpu().clone().pin_memory(), lens.cpu().clone().pin_memory()
-        hout = torch.empty(bufs.out.shape, dtype=torch.float32, **pin)
-        hsel = torch.empty(bufs.sel_ids.shape, dtype=torch.int32, **pin)
-        hdraw = torch.empty(bufs.draw_ids.shape, dtype=torch.int32, **pin)
-        hcnt = torch.empty(bufs.sel_count.shape, dtype=torch.int32, **pin)
-        hpi = torch.empty(bufs.pi.shape, dtype=torch.float32, **pin)
-        dq, dpt, dlens = torch.empty_like(q), torch.empty_like(pt), torch.empty_like(lens)
-        h2d = hq.numel() * hq.element_size() + hpt.numel() * 4 + hlens.numel() * 4
-        d2h = sum(x.numel() * x.element_size() for x in (hout, hsel, hdraw, hcnt, hpi))
+        inp = santa.StepInputs.allocate(q.dtype, cfg.batch, cfg.q_heads, d, n_teams, dev)
+        inp.host_q.copy_(q.cpu())
+        inp.host_page_table.copy_(pt.cpu())
+        inp.host_seq_lens.copy_(lens.cpu())
+        pbufs = santa.DecodeBuffers.allocate(q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads, d,
+                                             T, n_teams, M, dev, packed=True)
+        host = pbufs.host_mirror()
+        preps = [santa.santa_decode_prepared(inp.q, ks[r], vs[r], reps[r], inp.page_table,
+                                             inp.seq_lens, M, bufs=pbufs, sampler=args.sampler,
+                                             mix_alpha=args.mix_alpha) for r in range(R)]
+        h2d = inp.host_slab.numel()
+        d2h = host.slab.numel()
         K_e = max(20, min(K, 2000))
 
         def e2e_step(s):
-            r = s % R
-            with torch.cuda.stream(stream):
-                dq.copy_(hq, non_blocking=True)
-                dpt.copy_(hpt, non_blocking=True)
-                dlens.copy_(hlens, non_blocking=True)
-                santa.santa_decode(dq, ks[r], vs[r], reps[r], dpt, dlens, M, s, bufs=bufs,
-                                   stream=stream, sampler=args.sampler,
-                                   mix_alpha=args.mix_alpha)
-                hout.copy_(bufs.out, non_blocking=True)
-                hsel.copy_(bufs.sel_ids, non_blocking=True)
-                hdraw.copy_(bufs.draw_ids, non_blocking=True)
-                hcnt.copy_(bufs.sel_count, non_blocking=True)
-                hpi.copy_(bufs.pi, non_blocking=True)
+            inp.upload(stream)
+            preps[s % R].run(s, stream)
+            pbufs.download(host, stream)
             stream.synchronize()
 
         for s in range(W_):
@@ -497,7 +503,12 @@ def run_ours(args):
         "speedup_vs_dense": dense_s / step_s,
         "kernels_us": {"decode": step_s * 1e6, "sample_only": smp_s * 1e6,
                        "attend_only": att_s * 1e6, "dense": dense_s * 1e6,
-                       "append_token": append_us},
+                       "append_token": append_us, "build_reps": reps_us},
+        "build_reps": {"us": reps_us, "bytes": reps_bytes,
+                       "hbm_gbs": reps_bytes / reps_us / 1e3,
+                       "frac": reps_bytes / reps_us / 1e3 / peak,
+                       "note": "all valid keys read once, fp32 representatives written; "
+                               "once per prefill, not per step"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": "decode_kernel (fused sampling + split-K HT attention), "

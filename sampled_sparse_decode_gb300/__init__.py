@@ -14,7 +14,7 @@ _BINDING_NAMES = (
     "santa_dense_workspace_bytes", "santa_abi_version", "santa_status_string", "DecodeBuffers",
     "santa_decode_noalloc", "santa_noalloc_scratch_bytes", "santa_decode_plan",
     "SantaError", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_BAD_SEL", "santa_append_kv", "SAMPLERS",
-    "santa_attend_vs",
+    "santa_attend_vs", "StepInputs", "HostOutputs", "PreparedDecode", "santa_decode_prepared",
 )
 
 __all__ = list(_BINDING_NAMES) + ["workloads"]

@@ -181,6 +181,61 @@ def santa_update_reps(k_pool: torch.Tensor, pages: torch.Tensor, reps: torch.Ten
     return reps
 
 
+def _carve(slab: torch.Tensor, specs):
+    """Views of a flat uint8 tensor: one per (shape, dtype) in specs, each starting on a
+    16-byte boundary, in order."""
+    views, off = [], 0
+    for shape, dtype in specs:
+        n = 1
+        for x in shape:
+            n *= x
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        views.append(slab[off:off + nbytes].view(dtype).view(shape))
+        off += (nbytes + 15) // 16 * 16
+    return views
+
+
+def _packed_bytes(specs) -> int:
+    total = 0
+    for shape, dtype in specs:
+        n = 1
+        for x in shape:
+            n *= x
+        total += (n * torch.empty((), dtype=dtype).element_size() + 15) // 16 * 16
+    return total
+
+
+def _host_slab(nbytes: int) -> torch.Tensor:
+    """Page-locked when a GPU is present (asynchronous copies), plain memory otherwise."""
+    return torch.empty(nbytes, dtype=torch.uint8, pin_memory=torch.cuda.is_available())
+
+
+def _output_specs(batch, num_q_heads, num_kv_heads, head_dim, num_draws):
+    B, Hkv, M = batch, num_kv_heads, max(num_draws, 1)
+    return [((B, num_q_heads, head_dim), torch.float32), ((B, Hkv, M), torch.int32),
+            ((B, Hkv, M), torch.int32), ((B, Hkv), torch.int32), ((B, Hkv, M), torch.float32)]
+
+
+def _output_views(batch, num_q_heads, num_kv_heads, head_dim, num_draws, device, packed):
+    """(out, draw_ids, sel_ids, sel_count, pi) and their slab (None unless packed)."""
+    specs = _output_specs(batch, num_q_heads, num_kv_heads, head_dim, num_draws)
+    if not packed:
+        return [torch.empty(shape, dtype=dt, device=device) for shape, dt in specs], None
+    slab = torch.empty(_packed_bytes(specs), dtype=torch.uint8, device=device)
+    return _carve(slab, specs), slab
+
+
+@dataclass
+class HostOutputs:
+    """Page-locked host copies of a packed DecodeBuffers' five outputs (views of `slab`)."""
+    out: torch.Tensor
+    draw_ids: torch.Tensor
+    sel_ids: torch.Tensor
+    sel_count: torch.Tensor
+    pi: torch.Tensor
+    slab: torch.Tensor
+
+
 @dataclass
 class DecodeBuffers:
     """Outputs and scratch of one decode step for a fixed shape (reusable across steps)."""
@@ -192,11 +247,16 @@ class DecodeBuffers:
     team_probs: torch.Tensor | None   # [B][Hkv][max_teams] float32
     workspace: torch.Tensor    # uint8
     device_status: torch.Tensor  # [1] int32
+    outputs: torch.Tensor | None = None   # packed: the five outputs above as one uint8 slab
 
     @staticmethod
     def allocate(dtype, batch, num_q_heads, num_kv_heads, head_dim, team_size, max_teams,
-                 num_draws, device="cuda", team_probs=False, dense=False) -> "DecodeBuffers":
-        """dtype of q/K/V (torch.float32 or torch.bfloat16); sizes as in santa.h."""
+                 num_draws, device="cuda", team_probs=False, dense=False,
+                 packed=False) -> "DecodeBuffers":
+        """dtype of q/K/V (torch.float32 or torch.bfloat16); sizes as in santa.h.  With
+        packed=True, out, draw_ids, sel_ids, sel_count and pi are views of one slab
+        (`outputs`, each view 16-byte aligned), so one copy brings them all to the host
+        (host_mirror / download)."""
         B, Hkv, M = batch, num_kv_heads, max(num_draws, 1)
         ws = (santa_dense_workspace_bytes(dtype, B, num_q_heads, Hkv, head_dim, team_size,
                                           max_teams)
@@ -206,21 +266,103 @@ class DecodeBuffers:
         if ws == 0:
             raise SantaError("unsupported shape for the workspace query")
         i32 = dict(dtype=torch.int32, device=device)
+        views, slab = _output_views(B, num_q_heads, Hkv, head_dim, M, device, packed)
         return DecodeBuffers(
-            out=torch.empty((B, num_q_heads, head_dim), dtype=torch.float32, device=device),
-            draw_ids=torch.empty((B, Hkv, M), **i32),
-            sel_ids=torch.empty((B, Hkv, M), **i32),
-            sel_count=torch.empty((B, Hkv), **i32),
-            pi=torch.empty((B, Hkv, M), dtype=torch.float32, device=device),
+            out=views[0], draw_ids=views[1], sel_ids=views[2], sel_count=views[3], pi=views[4],
             team_probs=(torch.empty((B, Hkv, max_teams), dtype=torch.float32, device=device)
                         if team_probs else None),
             workspace=torch.zeros(ws, dtype=torch.uint8, device=device),
             device_status=torch.zeros(1, **i32),
+            outputs=slab,
         )
+
+    def host_mirror(self) -> HostOutputs:
+        """Host buffers with the packed layout of this DecodeBuffers (packed=True only)."""
+        if self.outputs is None:
+            raise SantaError("host_mirror needs DecodeBuffers.allocate(..., packed=True)")
+        B, Hq, d = self.out.shape
+        _, Hkv, M = self.pi.shape
+        specs = _output_specs(B, Hq, Hkv, d, M)
+        slab = _host_slab(self.outputs.numel())
+        return HostOutputs(*_carve(slab, specs), slab=slab)
+
+    def download(self, host: HostOutputs, stream=None) -> HostOutputs:
+        """One asynchronous device->host copy of all five outputs into `host` on `stream`
+        (the current stream by default); synchronise before reading it."""
+        if self.outputs is None or host.slab.numel() != self.outputs.numel():
+            raise SantaError("download needs a packed DecodeBuffers and its host_mirror()")
+        if stream is None:
+            host.slab.copy_(self.outputs, non_blocking=True)
+        else:
+            with torch.cuda.stream(stream):
+                host.slab.copy_(self.outputs, non_blocking=True)
+        return host
 
     def status(self) -> int:
         """Synchronise with the device and return the device status word."""
         return int(self.device_status.item())
+
+
+@dataclass
+class StepInputs:
+    """The per-step inputs q [B][Hq][d], page_table [B][max_teams] and seq_lens [B] as views
+    of one device slab, with host buffers of the same layout (host_q, host_page_table,
+    host_seq_lens), so that one copy uploads a step's inputs."""
+    q: torch.Tensor
+    page_table: torch.Tensor
+    seq_lens: torch.Tensor
+    host_q: torch.Tensor
+    host_page_table: torch.Tensor
+    host_seq_lens: torch.Tensor
+    slab: torch.Tensor
+    host_slab: torch.Tensor
+
+    @staticmethod
+    def allocate(dtype, batch, num_q_heads, head_dim, max_teams, device="cuda") -> "StepInputs":
+        specs = [((batch, num_q_heads, head_dim), dtype), ((batch, max_teams), torch.int32),
+                 ((batch,), torch.int32)]
+        nbytes = _packed_bytes(specs)
+        slab = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        host = _host_slab(nbytes)
+        return StepInputs(*_carve(slab, specs), *_carve(host, specs), slab=slab,
+                          host_slab=host)
+
+    def upload(self, stream=None) -> "StepInputs":
+        """One asynchronous host->device copy of the three host buffers on `stream`."""
+        if stream is None:
+            self.slab.copy_(self.host_slab, non_blocking=True)
+        else:
+            with torch.cuda.stream(stream):
+                self.slab.copy_(self.host_slab, non_blocking=True)
+        return self
+
+
+class PreparedDecode:
+    """santa_decode with its arguments checked and marshalled once, for steps that reuse
+    the same tensors (a decode loop over persistent buffers).  run(seed) changes only the
+    seed; the tensors' contents may change between runs, their storage may not."""
+
+    def __init__(self, q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int,
+                 bufs: DecodeBuffers | None = None, sampler: str = "iid_ht",
+                 mix_alpha: float = 0.0, team_probs: bool = False):
+        self.bufs = _bufs_for(q, k_pool, page_table, num_draws, bufs, team_probs)
+        self._keep = (q, k_pool, v_pool, reps, page_table, seq_lens)
+        self._a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, 0,
+                        self.bufs, sampler, mix_alpha)
+        self._fn = lib().santa_decode
+
+    def run(self, seed: int, stream=None) -> DecodeBuffers:
+        self._a.seed = seed & 0xFFFFFFFFFFFFFFFF
+        _check(self._fn(ctypes.byref(self._a), _stream(stream)), "santa_decode")
+        return self.bufs
+
+
+def santa_decode_prepared(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int,
+                          bufs: DecodeBuffers | None = None, sampler: str = "iid_ht",
+                          mix_alpha: float = 0.0, team_probs: bool = False) -> PreparedDecode:
+    """A PreparedDecode: santa_decode's checks and argument structure done once."""
+    return PreparedDecode(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, bufs,
+                          sampler, mix_alpha, team_probs)
 
 
 def _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed,

@@ -1,0 +1,61 @@
+"""The binding's fast path for decode loops: PreparedDecode (arguments marshalled once),
+packed DecodeBuffers with a host mirror, and StepInputs.  The kernel and its arguments are
+the same as santa_decode's, so the results must be bit-identical to santa_decode's."""
+import numpy as np
+import pytest
+import torch
+
+import sampled_sparse_decode_gb300 as santa
+from sampled_sparse_decode_gb300 import workloads as W
+from helpers import DeviceWorkload
+
+pytestmark = pytest.mark.gpu
+
+
+def _same(a, b):
+    for f in ("out", "draw_ids", "sel_ids", "sel_count", "pi"):
+        x, y = getattr(a, f), getattr(b, f)
+        if f in ("sel_ids", "pi"):       # only the first sel_count slots are defined
+            cnt = a.sel_count
+            m = torch.arange(x.shape[-1], device=x.device) < cnt[..., None]
+            x, y = x[m], y[m]
+        assert torch.equal(x, y), f
+
+
+def test_prepared_packed_matches_santa_decode():
+    wl = W.generate("qwen7b_32k_b8_m64", batch=3, seq_len=5000)
+    dw = DeviceWorkload(wl)
+    cfg = wl.cfg
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    inp = santa.StepInputs.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.head_dim,
+                                    wl.max_teams)
+    inp.host_q.copy_(dw.q.cpu())
+    inp.host_page_table.copy_(dw.page_table.cpu())
+    inp.host_seq_lens.copy_(dw.seq_lens.cpu())
+    inp.upload()
+    pbufs = santa.DecodeBuffers.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads,
+                                         cfg.head_dim, cfg.team_size, wl.max_teams, cfg.draws,
+                                         packed=True)
+    prep = santa.santa_decode_prepared(inp.q, dw.k_pool, dw.v_pool, reps, inp.page_table,
+                                       inp.seq_lens, cfg.draws, bufs=pbufs)
+    host = pbufs.host_mirror()
+    for seed in (0, 7, 123456789012345):
+        prep.run(seed)
+        pbufs.download(host)
+        ref = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
+                                 cfg.draws, seed)
+        torch.cuda.synchronize()
+        assert pbufs.status() == 0 and ref.status() == 0
+        _same(pbufs, ref)
+        for f in ("out", "draw_ids", "sel_ids", "sel_count", "pi"):
+            assert torch.equal(getattr(host, f), getattr(pbufs, f).cpu()), f
+    # new query contents through the same storage
+    q2 = W.f32_to_bf16_bits(np.random.default_rng(3).standard_normal(wl.q.shape)
+                            .astype(np.float32))
+    inp.host_q.copy_(torch.from_numpy(q2.view(np.int16)).view(torch.bfloat16))
+    inp.upload()
+    prep.run(11)
+    ref = santa.santa_decode(inp.q.clone(), dw.k_pool, dw.v_pool, reps, dw.page_table,
+                             dw.seq_lens, cfg.draws, 11)
+    torch.cuda.synchronize()
+    _same(pbufs, ref)
