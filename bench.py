@@ -15,10 +15,10 @@ value      steps/s of whole decode steps with inputs resident in HBM, K steps re
 roofline   the fused decode kernel (one launch per step): algorithmic bytes per launch (the
            team representatives, K and V of the sampled teams, q, out) / its mean duration
            (CUDA events over graph-replayed launches), against the measured HBM copy bandwidth.
-e2e        the same steps through the Python API with pinned host buffers: per step one
-           copy takes the query, page table and lengths host->device (StepInputs), a
-           PreparedDecode runs the step, one copy brings out, draw/sampled ids, pi and |S|
-           back device->host (packed DecodeBuffers), then the stream is synchronised.
+e2e        the same steps through the C ABI with pinned host buffers: per step one call of
+           santa_decode_host copies the query, page table and lengths host->device
+           (StepInputs), runs the decode, copies out, draw/sampled ids, pi, |S| and the
+           status word back device->host (packed DecodeBuffers) and waits for the stream.
 dense      the in-run dense split-K decode kernel on the same buffers (speed reference).
 cpu_baseline  the fp64 C oracle, single-threaded, on a bounded sample of steps.
 --impl reference  times that oracle alone (the reference arm of this benchmark).
@@ -434,10 +434,10 @@ def run_ours(args):
     acc = accuracy_vs_dense(q, ks[0], vs[0], reps[0], pt, lens, M, args.sampler, args.mix_alpha,
                             32, santa)
 
-    # ---- end to end through the Python API, host buffers: per step one host->device copy
-    # of the step's inputs (StepInputs), the decode (PreparedDecode over the rotation's
-    # buffers), one device->host copy of the five outputs (packed DecodeBuffers) and a
-    # stream synchronisation
+    # ---- end to end through the Python API, host buffers: per step one call of
+    # santa_decode_host (PreparedDecode.run_host over the rotation's buffers): one
+    # host->device copy of the step's inputs (StepInputs), the decode, one device->host copy
+    # of the outputs and status word (packed DecodeBuffers), and the wait for the stream
     e2e = None
     if not args.no_e2e:
         inp = santa.StepInputs.allocate(q.dtype, cfg.batch, cfg.q_heads, d, n_teams, dev)
@@ -455,10 +455,7 @@ def run_ours(args):
         K_e = max(20, min(K, 2000))
 
         def e2e_step(s):
-            inp.upload(stream)
-            preps[s % R].run(s, stream)
-            pbufs.download(host, stream)
-            stream.synchronize()
+            preps[s % R].run_host(s, inp, host, stream)
 
         for s in range(W_):
             e2e_step(s)
@@ -468,6 +465,7 @@ def run_ours(args):
             e2e_step(W_ + s)
         el = time.perf_counter() - t0
         e2e_rate, el = job_rate(el, K_e, world, dev)
+        assert int(host.device_status[0]) == 0
         e2e = {"value": e2e_rate, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": K_e}
 

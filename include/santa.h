@@ -294,6 +294,29 @@ int santa_dense_decode(const santa_decode_args* a, void* stream);
 int santa_decode_noalloc(const santa_decode_args* a, void* stream);
 
 /*
+ * santa_decode_host — one decode step whose inputs come from and whose outputs go to host
+ * memory (no counterpart in the paper; a convenience of this library).  On `stream` it
+ * copies in_bytes from host_in to dev_in, runs santa_decode(a), copies out_bytes from
+ * dev_out to host_out and waits for the stream.
+ *
+ *   - The caller lays out the buffers.  a's input pointers (q, page_table, seq_lens) point
+ *     into dev_in, and its output pointers (out, draw_ids, sel_ids, sel_count, pi, and
+ *     device_status if the caller wants it back in the same copy) into dev_out, so that
+ *     one copy moves each side.  The library reads neither layout: it copies bytes.
+ *   - host_in and host_out should be page-locked (cudaHostAlloc or a pinned torch tensor).
+ *     Pageable memory works, but then the runtime stages the copies synchronously.
+ *   - in_bytes or out_bytes may be 0 (that copy is skipped); otherwise both pointers of
+ *     that copy must be non-null (SANTA_ERR_INVALID_ARG, nothing enqueued).
+ *   - Returns santa_decode's error if the step is refused (the input copy may already be
+ *     enqueued), SANTA_ERR_CUDA if a copy or the stream wait fails, else SANTA_OK after the
+ *     host outputs are complete.  device_status is not read here; with device_status in
+ *     dev_out, the caller reads the host copy.
+ */
+int santa_decode_host(const santa_decode_args* a, const void* host_in, void* dev_in,
+                      size_t in_bytes, void* host_out, const void* dev_out, size_t out_bytes,
+                      void* stream);
+
+/*
  * santa_attend_vs — santa_attend with value-row sampling inside every listed team, in place
  * of the full P.V product ([SANTA] "Stochastic Sparse Attention for Memory-Bound
  * Inference", abstract: draw value rows from the post-softmax distribution and gather-add

@@ -77,6 +77,7 @@ def lib():
             "santa_decode": (i32, [A, vp]),
             "santa_dense_decode": (i32, [A, vp]),
             "santa_decode_noalloc": (i32, [A, vp]),
+            "santa_decode_host": (i32, [A, vp, vp, sz, vp, vp, sz, vp]),
             "santa_decode_plan": (i32, [A, i32, vp]),
             "santa_noalloc_scratch_bytes": (sz, []),
         }
@@ -211,28 +212,33 @@ def _host_slab(nbytes: int) -> torch.Tensor:
 
 
 def _output_specs(batch, num_q_heads, num_kv_heads, head_dim, num_draws):
+    """out, draw_ids, sel_ids, sel_count, pi and the device status word."""
     B, Hkv, M = batch, num_kv_heads, max(num_draws, 1)
     return [((B, num_q_heads, head_dim), torch.float32), ((B, Hkv, M), torch.int32),
-            ((B, Hkv, M), torch.int32), ((B, Hkv), torch.int32), ((B, Hkv, M), torch.float32)]
+            ((B, Hkv, M), torch.int32), ((B, Hkv), torch.int32), ((B, Hkv, M), torch.float32),
+            ((1,), torch.int32)]
 
 
 def _output_views(batch, num_q_heads, num_kv_heads, head_dim, num_draws, device, packed):
-    """(out, draw_ids, sel_ids, sel_count, pi) and their slab (None unless packed)."""
+    """(out, draw_ids, sel_ids, sel_count, pi, device_status) and their slab (None unless
+    packed).  The status word starts at zero."""
     specs = _output_specs(batch, num_q_heads, num_kv_heads, head_dim, num_draws)
     if not packed:
-        return [torch.empty(shape, dtype=dt, device=device) for shape, dt in specs], None
-    slab = torch.empty(_packed_bytes(specs), dtype=torch.uint8, device=device)
+        views = [torch.empty(shape, dtype=dt, device=device) for shape, dt in specs[:-1]]
+        return views + [torch.zeros(1, dtype=torch.int32, device=device)], None
+    slab = torch.zeros(_packed_bytes(specs), dtype=torch.uint8, device=device)
     return _carve(slab, specs), slab
 
 
 @dataclass
 class HostOutputs:
-    """Page-locked host copies of a packed DecodeBuffers' five outputs (views of `slab`)."""
+    """Host copies of a packed DecodeBuffers' outputs and status word (views of `slab`)."""
     out: torch.Tensor
     draw_ids: torch.Tensor
     sel_ids: torch.Tensor
     sel_count: torch.Tensor
     pi: torch.Tensor
+    device_status: torch.Tensor
     slab: torch.Tensor
 
 
@@ -254,8 +260,8 @@ class DecodeBuffers:
                  num_draws, device="cuda", team_probs=False, dense=False,
                  packed=False) -> "DecodeBuffers":
         """dtype of q/K/V (torch.float32 or torch.bfloat16); sizes as in santa.h.  With
-        packed=True, out, draw_ids, sel_ids, sel_count and pi are views of one slab
-        (`outputs`, each view 16-byte aligned), so one copy brings them all to the host
+        packed=True, out, draw_ids, sel_ids, sel_count, pi and device_status are views of one
+        slab (`outputs`, each view 16-byte aligned), so one copy brings them all to the host
         (host_mirror / download)."""
         B, Hkv, M = batch, num_kv_heads, max(num_draws, 1)
         ws = (santa_dense_workspace_bytes(dtype, B, num_q_heads, Hkv, head_dim, team_size,
@@ -265,14 +271,13 @@ class DecodeBuffers:
                                            max_teams, M))
         if ws == 0:
             raise SantaError("unsupported shape for the workspace query")
-        i32 = dict(dtype=torch.int32, device=device)
         views, slab = _output_views(B, num_q_heads, Hkv, head_dim, M, device, packed)
         return DecodeBuffers(
             out=views[0], draw_ids=views[1], sel_ids=views[2], sel_count=views[3], pi=views[4],
             team_probs=(torch.empty((B, Hkv, max_teams), dtype=torch.float32, device=device)
                         if team_probs else None),
             workspace=torch.zeros(ws, dtype=torch.uint8, device=device),
-            device_status=torch.zeros(1, **i32),
+            device_status=views[5],
             outputs=slab,
         )
 
@@ -287,7 +292,7 @@ class DecodeBuffers:
         return HostOutputs(*_carve(slab, specs), slab=slab)
 
     def download(self, host: HostOutputs, stream=None) -> HostOutputs:
-        """One asynchronous device->host copy of all five outputs into `host` on `stream`
+        """One asynchronous device->host copy of the outputs and status into `host` on `stream`
         (the current stream by default); synchronise before reading it."""
         if self.outputs is None or host.slab.numel() != self.outputs.numel():
             raise SantaError("download needs a packed DecodeBuffers and its host_mirror()")
@@ -355,6 +360,26 @@ class PreparedDecode:
         self._a.seed = seed & 0xFFFFFFFFFFFFFFFF
         _check(self._fn(ctypes.byref(self._a), _stream(stream)), "santa_decode")
         return self.bufs
+
+    def run_host(self, seed: int, inputs: StepInputs, host: HostOutputs,
+                 stream=None) -> HostOutputs:
+        """One step through santa_decode_host: inputs.host_slab -> inputs.slab, the decode,
+        bufs.outputs -> host.slab, then a wait for the stream.  The PreparedDecode must have
+        been made on inputs' device views and packed DecodeBuffers; host.device_status holds
+        the step's status word (sticky: zero it in the device slab to clear it)."""
+        b = self.bufs
+        if (b.outputs is None or host.slab.numel() != b.outputs.numel() or
+                self._a.q != inputs.q.data_ptr() or
+                self._a.page_table != inputs.page_table.data_ptr() or
+                self._a.seq_lens != inputs.seq_lens.data_ptr()):
+            raise SantaError("run_host needs packed DecodeBuffers, their host_mirror() and a "
+                             "PreparedDecode made on the StepInputs' device views")
+        self._a.seed = seed & 0xFFFFFFFFFFFFFFFF
+        _check(lib().santa_decode_host(ctypes.byref(self._a), inputs.host_slab.data_ptr(),
+                                       inputs.slab.data_ptr(), inputs.slab.numel(),
+                                       host.slab.data_ptr(), b.outputs.data_ptr(),
+                                       b.outputs.numel(), _stream(stream)), "santa_decode_host")
+        return host
 
 
 def santa_decode_prepared(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int,

@@ -586,5 +586,22 @@ int santa_dense_decode(const santa_decode_args* a, void* stream) {
   return launch(a, santa::kModeDense, static_cast<cudaStream_t>(stream));
 }
 
+int santa_decode_host(const santa_decode_args* a, const void* host_in, void* dev_in,
+                      size_t in_bytes, void* host_out, const void* dev_out, size_t out_bytes,
+                      void* stream) {
+  if (!a || (in_bytes && (!host_in || !dev_in)) || (out_bytes && (!host_out || !dev_out)))
+    return SANTA_ERR_INVALID_ARG;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (in_bytes &&
+      cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return SANTA_ERR_CUDA;
+  const int rc = launch(a, santa::kModeDecode, s);
+  if (rc != SANTA_OK) return rc;
+  if (out_bytes &&
+      cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SANTA_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
+}
+
 }  // extern "C"
 #pragma GCC visibility pop

@@ -78,6 +78,19 @@ def test_null_args(lib):
     assert lib.santa_decode(ctypes.byref(a), None) == INVALID
 
 
+def test_host_step_rejects_missing_buffers(lib):
+    f = lib.santa_decode_host
+    f.restype = ctypes.c_int
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    f.argtypes = [ctypes.c_void_p, vp, vp, sz, vp, vp, sz, vp]
+    a = valid_args()
+    assert f(None, 0x1000, 0x2000, 16, 0x3000, 0x4000, 16, None) == INVALID
+    assert f(ctypes.addressof(a), None, 0x2000, 16, 0x3000, 0x4000, 16, None) == INVALID
+    assert f(ctypes.addressof(a), 0x1000, None, 16, 0x3000, 0x4000, 16, None) == INVALID
+    assert f(ctypes.addressof(a), 0x1000, 0x2000, 16, None, 0x4000, 16, None) == INVALID
+    assert f(ctypes.addressof(a), 0x1000, 0x2000, 16, 0x3000, None, 16, None) == INVALID
+
+
 def test_reps_reject_bad_arguments_on_host(lib):
     f = lib.santa_build_reps
     f.restype = ctypes.c_int

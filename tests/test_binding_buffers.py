@@ -1,5 +1,5 @@
 """Packed step buffers of the binding (CPU): DecodeBuffers(packed=True) carves the five
-outputs out of one slab, host_mirror() gives host buffers of the same layout, and
+outputs and the device status word out of one slab, host_mirror() gives host buffers of the same layout, and
 StepInputs does the same for a step's inputs, so one copy moves each side.  Checked here:
 shapes and dtypes, 16-byte alignment of every view, no overlap, and that a copy of the slab
 moves every view's contents."""
@@ -25,9 +25,10 @@ def _views_ok(slab, views):
 def _packed(B, Hq, Hkv, d, M, packed=True):
     """The outputs as DecodeBuffers.allocate lays them out (the workspace size query needs a
     GPU, so the scratch fields are stand-ins here)."""
-    views, slab = Bn._output_views(B, Hq, Hkv, d, M, "cpu", packed)
-    return Bn.DecodeBuffers(*views, team_probs=None, workspace=torch.zeros(16, dtype=torch.uint8),
-                            device_status=torch.zeros(1, dtype=torch.int32), outputs=slab)
+    v, slab = Bn._output_views(B, Hq, Hkv, d, M, "cpu", packed)
+    return Bn.DecodeBuffers(out=v[0], draw_ids=v[1], sel_ids=v[2], sel_count=v[3], pi=v[4],
+                            team_probs=None, workspace=torch.zeros(16, dtype=torch.uint8),
+                            device_status=v[5], outputs=slab)
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,d,M", [(3, 28, 4, 128, 31), (1, 2, 1, 64, 7)])
@@ -38,18 +39,22 @@ def test_packed_outputs_layout_and_round_trip(B, Hq, Hkv, d, M):
                                               (B, Hkv, M)]
     assert [x.dtype for x in outs] == [torch.float32, torch.int32, torch.int32, torch.int32,
                                        torch.float32]
-    _views_ok(bufs.outputs, outs)
+    _views_ok(bufs.outputs, outs + [bufs.device_status])
+    assert bufs.device_status.shape == (1,) and int(bufs.device_status[0]) == 0
     g = torch.Generator().manual_seed(1)
     bufs.out.copy_(torch.randn(bufs.out.shape, generator=g))
     bufs.draw_ids.copy_(torch.randint(0, 99, bufs.draw_ids.shape, generator=g))
     bufs.sel_ids.copy_(torch.randint(0, 99, bufs.sel_ids.shape, generator=g))
     bufs.sel_count.copy_(torch.randint(0, 99, bufs.sel_count.shape, generator=g))
     bufs.pi.copy_(torch.rand(bufs.pi.shape, generator=g))
+    bufs.device_status.fill_(5)
     host = bufs.host_mirror()
-    _views_ok(host.slab, [host.out, host.draw_ids, host.sel_ids, host.sel_count, host.pi])
+    _views_ok(host.slab, [host.out, host.draw_ids, host.sel_ids, host.sel_count, host.pi,
+                          host.device_status])
     bufs.download(host)
     for a, b in zip(outs, [host.out, host.draw_ids, host.sel_ids, host.sel_count, host.pi]):
         assert torch.equal(a, b)
+    assert int(host.device_status[0]) == 5
 
 
 def test_unpacked_buffers_have_no_mirror():

@@ -59,3 +59,42 @@ def test_prepared_packed_matches_santa_decode():
                              dw.seq_lens, cfg.draws, 11)
     torch.cuda.synchronize()
     _same(pbufs, ref)
+
+
+def test_host_step_matches_santa_decode():
+    """santa_decode_host through PreparedDecode.run_host: one upload, the decode, one
+    download of outputs and status, and the wait, all in one call."""
+    wl = W.generate("llama8b_paged_32k_b16_m32", batch=2, seq_len=3000, num_pages=64)
+    dw = DeviceWorkload(wl)
+    cfg = wl.cfg
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    inp = santa.StepInputs.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.head_dim,
+                                    wl.max_teams)
+    inp.host_q.copy_(dw.q.cpu())
+    inp.host_page_table.copy_(dw.page_table.cpu())
+    inp.host_seq_lens.copy_(dw.seq_lens.cpu())
+    pbufs = santa.DecodeBuffers.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads,
+                                         cfg.head_dim, cfg.team_size, wl.max_teams, cfg.draws,
+                                         packed=True)
+    host = pbufs.host_mirror()
+    prep = santa.santa_decode_prepared(inp.q, dw.k_pool, dw.v_pool, reps, inp.page_table,
+                                       inp.seq_lens, cfg.draws, bufs=pbufs)
+    for seed in (1, 2):
+        prep.run_host(seed, inp, host)
+        assert int(host.device_status[0]) == 0
+        ref = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
+                                 cfg.draws, seed)
+        torch.cuda.synchronize()
+        for f in ("out", "draw_ids", "sel_count"):
+            assert torch.equal(getattr(host, f), getattr(ref, f).cpu()), f
+        cnt = host.sel_count
+        m = torch.arange(cfg.draws) < cnt[..., None]
+        assert torch.equal(host.sel_ids[m], ref.sel_ids.cpu()[m])
+        assert torch.equal(host.pi[m], ref.pi.cpu()[m])
+    # a bad page id reaches the host through the packed status word
+    inp.host_page_table[1, 0] = dw.k_pool.shape[0] + 5
+    prep.run_host(3, inp, host)
+    assert int(host.device_status[0]) & santa.DEV_BAD_PAGE
+    with pytest.raises(santa.SantaError):
+        santa.santa_decode_prepared(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table,
+                                    dw.seq_lens, cfg.draws, bufs=pbufs).run_host(1, inp, host)
