@@ -111,6 +111,21 @@ def test_workspace_of_minimum_size():
         assert (full.out - small.out).abs().max().item() <= 1e-5
 
 
+def test_maximum_team_count():
+    """The largest supported cache per sequence: max_teams = 16384 teams of 64 tokens
+    (1M tokens, bf16, d = 64).  The sampling takes the largest cluster, 16 CTAs of 1024
+    teams each, the most one CTA scores.  S and the output match the oracle for M = 64 and
+    for the largest M, 4096 (whose sampled teams also span several clusters)."""
+    wl = W.generate("tiny_f32", seq_len=16384 * 64, dtype="bf16", draws=64)
+    assert wl.max_teams == 16384
+    dw = DeviceWorkload(wl)
+    plan = santa.santa_decode_plan(dw.q, dw.k_pool, dw.page_table, 64, "decode")
+    assert plan["cluster"] == 16 and plan["teams_per_cta"] == 1024, plan
+    for M, seed in ((64, 5), (4096, 6)):
+        bufs, res = decode_vs_oracle(wl, M, seed)
+        assert res[0].sel.size == int(bufs.sel_count[0, 0]) > M // 2
+
+
 def test_repeated_calls_are_deterministic():
     """The workspace counters reset themselves: back-to-back calls on the same buffers give
     bit-identical outputs."""
