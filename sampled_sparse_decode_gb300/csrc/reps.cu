@@ -122,14 +122,14 @@ __global__ void __launch_bounds__(kRepThreads) reps_kernel(RepsParams p) {
 // its L % T + 1 valid keys.  The mean is summed exactly as reps_kernel sums it (same
 // thread split, same order: the new key is the last term of its row group), from the pool
 // rows already there plus the new key, so it equals santa_build_reps on the grown pool bit
-// for bit while reading only this page.  Launched with programmatic stream serialization:
-// it touches global memory only after the previous kernel of the stream has completed.
+// for bit while reading only this page.  It is launched plainly, not as a programmatic
+// dependent launch: that would let the next decode grid become resident beside these few
+// blocks, and at batch 8 its clusters then no longer fit the SMs in one wave (35-40% longer
+// decode steps in a generation loop, where the step itself gained nothing at batch 1).
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kRepThreads) append_kernel(AppendParams p) {
   using Sp = RepSplit<BF16, D>;
   __shared__ __align__(16) float part[Sp::kGroups * D];
-  grid_dependency_wait();
-  grid_launch_dependents();
   const int col = threadIdx.x % Sp::kCols;
   const int group = threadIdx.x / Sp::kCols;
   const int64_t items = static_cast<int64_t>(p.batch) * p.num_kv_heads;
@@ -176,20 +176,19 @@ __global__ void __launch_bounds__(kRepThreads) append_kernel(AppendParams p) {
 cudaError_t launch_append(const AppendParams& p, int head_dim, cudaStream_t stream) {
   const int64_t items = static_cast<int64_t>(p.batch) * p.num_kv_heads;
   if (items == 0) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(items < (1ll << 30) ? items : (1ll << 30)));
-  cfg.blockDim = dim3(kRepThreads);
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (p.is_bf16)
-    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, append_kernel<true, 128>, p)
-                           : cudaLaunchKernelEx(&cfg, append_kernel<true, 64>, p);
-  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, append_kernel<false, 128>, p)
-                         : cudaLaunchKernelEx(&cfg, append_kernel<false, 64>, p);
+  const unsigned grid = static_cast<unsigned>(items < (1ll << 30) ? items : (1ll << 30));
+  if (p.is_bf16) {
+    if (head_dim == 128)
+      append_kernel<true, 128><<<grid, kRepThreads, 0, stream>>>(p);
+    else
+      append_kernel<true, 64><<<grid, kRepThreads, 0, stream>>>(p);
+  } else {
+    if (head_dim == 128)
+      append_kernel<false, 128><<<grid, kRepThreads, 0, stream>>>(p);
+    else
+      append_kernel<false, 64><<<grid, kRepThreads, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_reps(const RepsParams& p, int head_dim, cudaStream_t stream) {
