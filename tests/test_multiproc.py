@@ -34,7 +34,7 @@ def _rank_main(rank, world, port, out):
 
 def test_job_rate_takes_the_slowest_rank():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()     # no fork of a threaded process
     mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
     for rank in range(world):
         rate, slowest = out[rank]
