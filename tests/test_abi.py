@@ -113,3 +113,84 @@ def test_minimum_workspace_size(lib):
     # + (m, l) [4][2][7][2] fp32 rounded to 256 + acc [4][2][7][128] fp32
     assert f(1, 28, 4, 128, 128, 16384, 4096) == 256 + 256 + 512 + 4 * 2 * 7 * 128 * 4
     assert f(1, 30, 4, 128, 128, 256, 31) == 0
+
+
+SCRATCH_LIMIT = 5
+
+
+def test_append_rejects_bad_arguments_on_host(lib):
+    f = lib.santa_append_kv
+    f.restype = ctypes.c_int
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    f.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    good = dict(k_new=0x10000, v_new=0x20000, dtype=1, batch=2, hkv=4, T=128, d=128, mt=256,
+                P=512, pt=0x30000, lens=0x40000, k=0x50000, v=0x60000, reps=0x70000,
+                nxt=0x80000, status=0x90000)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return f(a["k_new"], a["v_new"], a["dtype"], a["batch"], a["hkv"], a["T"], a["d"],
+                 a["mt"], a["P"], a["pt"], a["lens"], a["k"], a["v"], a["reps"], a["nxt"],
+                 a["status"], None)
+
+    assert call(dtype=7) == UNSUPPORTED
+    assert call(d=96) == UNSUPPORTED
+    assert call(T=32) == UNSUPPORTED
+    assert call(mt=20000) == UNSUPPORTED
+    assert call(batch=0) == INVALID
+    assert call(P=0) == INVALID
+    assert call(k_new=None) == INVALID
+    assert call(reps=None) == INVALID
+    assert call(k=0x50008) == INVALID                    # not 16-byte aligned
+    assert call(pt=0x30002) == INVALID
+    assert call(nxt=0x40000) == INVALID                  # lengths written while read
+
+
+def test_update_reps_needs_a_page_list(lib):
+    f = lib.santa_update_reps
+    f.restype = ctypes.c_int
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    f.argtypes = [vp, i32, i64, i32, i32, i32, vp, i32, vp, vp, vp, vp]
+    assert f(0x10000, 1, 16, 4, 128, 128, None, 3, None, 0x20000, None, None) == INVALID
+    assert f(0x10000, 1, 16, 4, 128, 128, 0x30002, 3, None, 0x20000, None, None) == INVALID
+
+
+def test_value_sampling_rejects_bad_arguments_on_host(lib):
+    f = lib.santa_attend_vs
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    ws = lib.santa_attend_vs_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [ctypes.c_int] * 5
+    a = valid_args()
+    need = ws(a.batch, a.num_q_heads, a.num_kv_heads, a.head_dim, a.num_draws)
+    assert need > 0
+    a.workspace, a.workspace_bytes = 0xA0000, need - 1
+    assert f(ctypes.byref(a), 16, None, None) == INVALID          # workspace one byte short
+    for rows in (0, 257):
+        assert f(ctypes.byref(a), rows, None, None) == UNSUPPORTED
+    a.num_draws = 2000
+    assert f(ctypes.byref(a), 16, None, None) == UNSUPPORTED
+    a = valid_args()
+    a.workspace, a.workspace_bytes = 0xA0000, need
+    a.out = 0x10008                                                 # out must be 16-byte aligned
+    assert f(ctypes.byref(a), 16, None, None) == INVALID
+    a = valid_args()
+    a.workspace, a.workspace_bytes = 0xA0000, need
+    assert f(ctypes.byref(a), 16, 0x30002, None) == INVALID         # value_ids misaligned
+    assert f(None, 16, None, None) == INVALID
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
+    f = lib.santa_decode_noalloc
+    f.restype = ctypes.c_int
+    lib.santa_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    assert lib.santa_noalloc_scratch_bytes() == 4 << 20
+    a = valid_args()
+    a.head_dim = 96
+    assert f(ctypes.byref(a), None) == UNSUPPORTED
+    # 4096 draws of 128-token teams over 16384 teams, 64 sequences x 8 heads: the split
+    # partials alone exceed the 4 MiB scratch
+    a = valid_args()
+    a.batch, a.num_q_heads, a.num_kv_heads, a.max_teams, a.num_draws = 64, 64, 8, 16384, 4096
+    assert f(ctypes.byref(a), None) == SCRATCH_LIMIT
