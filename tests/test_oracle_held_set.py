@@ -8,9 +8,11 @@ the grown cache.  Horvitz-Thompson stays unbiased for any per-team quantity, so 
 step's numerator and denominator are still unbiased for the dense sums over every team that
 existed at the refresh step.  That includes tokens appended to those teams later.  A team
 opened after the refresh has pi = 0 and is missing until the next refresh.  Both facts are
-checked by enumerating every ordered draw sequence on tiny inputs, against plain numpy sums.
+checked by enumerating every ordered draw sequence on tiny inputs, against plain numpy sums,
+and by a hand-derived example in exact rationals (tests/golden/worked_held_set.txt).
 """
 import itertools
+import os
 
 import numpy as np
 import pytest
@@ -88,3 +90,43 @@ def test_team_opened_after_the_refresh_is_missing_until_the_next():
     np.testing.assert_allclose(E_den, e[:, :20].sum(axis=1), rtol=1e-12)
     np.testing.assert_allclose(E_num, e[:, :20] @ V[:20], rtol=1e-12, atol=1e-12)
     assert np.all(np.abs(E_den - e.sum(axis=1)) >= 0.5 * e[:, 20])
+
+
+def _golden(name):
+    vals = {}
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if line:
+            k, v = line.split("=")
+            vals[k.strip()] = np.array([float(x) for x in v.split()])
+    return vals
+
+
+def test_worked_held_set_example():
+    """Hand-derived example (tests/golden/worked_held_set.txt): the two-team problem sampled
+    with q = 1, then held for a later query q' = 2.  Per-outcome estimates and their exact
+    expectations (the later query's dense sums)."""
+    g = _golden("worked_held_set.txt")
+    k = np.array(g["k"], np.float32).reshape(2, 1, 1, 1)
+    v = np.array(g["v"], np.float32).reshape(2, 1, 1, 1)
+    pt, lens = np.array([[0, 1]], np.int32), np.array([2], np.int32)
+    pr0 = oracle.Problem(np.array([[[g["q"][0]]]], np.float32), k, v, pt, lens)
+    p = oracle.team_probs(pr0, oracle.build_reps(pr0), 0, 0)
+    M = int(g["M"][0])
+    pi = np.array([oracle.select(np.full(M, i, np.int32), p)[1][0] for i in range(2)])
+    np.testing.assert_allclose(pi, g["pi"], rtol=1e-6)
+    pr1 = oracle.Problem(np.array([[[g["q_later"][0]]]], np.float32), k, v, pt, lens)
+    got = {}
+    for S, tag in [((0,), "S0"), ((1,), "S1"), ((0, 1), "S01")]:
+        num, den = oracle.num_den(pr1, 0, 0, np.array(S, np.int32), pi[list(S)], 0.0)
+        np.testing.assert_allclose([num[0, 0], den[0]], [g["num_" + tag][0], g["den_" + tag][0]],
+                                   rtol=1e-6)
+        got[S] = (num[0, 0], den[0])
+    E_num = E_den = 0.0
+    for seq in itertools.product(range(2), repeat=M):
+        prob = np.prod(p[list(seq)])
+        n_, d_ = got[tuple(sorted(set(seq)))]
+        E_num += prob * n_
+        E_den += prob * d_
+    np.testing.assert_allclose([E_num, E_den], [g["E_num"][0], g["E_den"][0]], rtol=1e-6)
