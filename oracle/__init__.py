@@ -51,9 +51,11 @@ _lib = None
 
 
 def lib():
+    """The oracle library: liboracle.so, or the library named by ORACLE_LIB (the mutation
+    tests load deliberately broken builds of oracle.c that way, to show the pins catch them)."""
     global _lib
     if _lib is None:
-        L = ctypes.CDLL(build())
+        L = ctypes.CDLL(os.environ.get("ORACLE_LIB") or build())
         P = ctypes.POINTER(_Problem)
         vp, i32, i64, u64, dbl = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                   ctypes.c_uint64, ctypes.c_double)
