@@ -374,6 +374,26 @@ def test_dense_special_case_all_pi_one():
     np.testing.assert_allclose(r.out, sdpa, rtol=0, atol=1e-12)
 
 
+def test_dense_special_case_every_kv_head():
+    """The all-pi-one case on every unit of a multi-head, multi-sequence, paged problem:
+    2 sequences of different lengths (partial last teams), 3 KV heads with G = 2, a permuted
+    page pool.  Each unit's estimate and the oracle's dense attention equal textbook softmax
+    attention over that unit's own keys and values (numpy, fp64)."""
+    cfg = _tiny(batch=2, q_heads=6, kv_heads=3, head_dim=8, team_size=8, paged=True,
+                num_pages=16, data_seed=21)
+    wl = W.generate(cfg, seq_lens=[37, 21], invalid_fill=float("nan"))
+    wl.q[:] = wl.q * np.float32(0.05)                  # near-uniform team distribution
+    pr = _problem(wl)
+    reps = oracle.build_reps(pr, wl.page_fill)
+    for b in range(2):
+        for h in range(3):
+            r = oracle.decode(pr, reps, 4096, 3, b, h)
+            assert r.sel.size == -(-int(wl.seq_lens[b]) // 8) and (r.pi == 1.0).all()
+            want = _dense_numpy(wl, b, h)
+            np.testing.assert_allclose(r.out, want, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(oracle.dense(pr, b, h), want, rtol=0, atol=1e-12)
+
+
 def test_single_team_sequence_is_exact():
     cfg = _tiny(seq_len=6, team_size=8, head_dim=8)
     wl = W.generate(cfg, invalid_fill=float("nan"))

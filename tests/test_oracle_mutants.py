@@ -42,6 +42,24 @@ MUTANTS = {
     "unweighted denominator": [("        den[g] += w * e;", "        den[g] += e;")],
     "padded slots counted in a partial team": [
         ("  return rest < pr->team_size ? rest : pr->team_size;", "  return pr->team_size;")],
+    "values read from KV head 0": [
+        ("          num[g * d + k] += w * e * elem(pr->v_pool, pr->dtype, kv_index(pr, page, h, t, k));",
+         "          num[g * d + k] += w * e * elem(pr->v_pool, pr->dtype, kv_index(pr, page, 0, t, k));")],
+    "token scores against keys of KV head 0": [
+        ("    dot += q_elem(pr, b, hq, k) * elem(pr->k_pool, pr->dtype, kv_index(pr, page, h, t, k));",
+         "    dot += q_elem(pr, b, hq, k) * elem(pr->k_pool, pr->dtype, kv_index(pr, page, 0, t, k));")],
+    "exclusive CDF": [
+        ("    run += oracle_fixed_prob(p[i]);\n    C[i] = run;",
+         "    C[i] = run;\n    run += oracle_fixed_prob(p[i]);")],
+    "inclusion probability of M - 1 draws": [
+        ("      pi[count] = -expm1((double)M * log1p(-p[i]));",
+         "      pi[count] = -expm1((double)(M - 1) * log1p(-p[i]));")],
+    "page table ignored": [
+        ("  return pr->page_table[(int64_t)b * pr->max_teams + i];",
+         "  return (int64_t)b * pr->max_teams + i;")],
+    "weight pi instead of 1/pi": [
+        ("      const double w = 1.0 / pi[c];\n      for (int t = 0; t < len; ++t) {",
+         "      const double w = pi[c];\n      for (int t = 0; t < len; ++t) {")],
     "draw uniform without the 1/2": [
         ("  oracle_philox4x32_10(ctr, key, w);\n"
          "  unsigned __int128 prod = (unsigned __int128)(2ull * w[0] + 1ull) * Z;\n"
