@@ -67,7 +67,22 @@ MUTANTS = {
          "  oracle_philox4x32_10(ctr, key, w);\n"
          "  unsigned __int128 prod = (unsigned __int128)(2ull * w[0]) * Z;\n"
          "  return (uint64_t)(prod >> 33);\n}\n\n/* M i.i.d. draws")],
+    "sampled set in descending order": [
+        ("  int count = 0;\n  for (int i = 0; i < n; ++i) {\n    int hit = 0;",
+         "  int count = 0;\n  for (int i = n - 1; i >= 0; --i) {\n    int hit = 0;")],
+    "team probabilities summed over the heads": [
+        ("  for (int i = 0; i < n; ++i) p[i] /= (double)G;", "")],
+    "bf16 read from the low half-word": [
+        ("    uint32_t w = (uint32_t)((const uint16_t*)base)[idx] << 16;",
+         "    uint32_t w = (uint32_t)((const uint16_t*)base)[idx];")],
     # the next rows
+    "systematic uniform from draw 1": [
+        ("  const uint64_t t_u = oracle_draw_point(seed, b, h, 0, Z);",
+         "  const uint64_t t_u = oracle_draw_point(seed, b, h, 1, Z);")],
+    "mixture left out of the whole step": [("  oracle_mix(q, n, alpha, q);\n", "")],
+    "value rows averaged without 1/S": [
+        ("token_score(pr, b, hq, h, page, j) - shift[g]) / r[j] / S;",
+         "token_score(pr, b, hq, h, page, j) - shift[g]) / r[j];")],
     "systematic weight without min(1, .)": [
         ("      recip[count] = fmin(1.0, (double)M * q[i]);", "      recip[count] = (double)M * q[i];")],
     "Hansen-Hurwitz weight ignores the draw count": [
