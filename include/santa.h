@@ -282,14 +282,21 @@ int santa_dense_decode(const santa_decode_args* a, void* stream);
  *   - Same inputs, outputs and results as santa_decode (the split plan is the default one
  *     cut down to fit the scratch, so the output may differ from santa_decode's in the
  *     last bits only).
- *   - Returns SANTA_ERR_SCRATCH_LIMIT, launching nothing, when the shape needs more than
- *     the scratch holds (santa_decode_workspace_min_bytes > santa_noalloc_scratch_bytes).
+ *   - Returns SANTA_ERR_SCRATCH_LIMIT, before any CUDA call, when the shape needs more than
+ *     the scratch holds: santa_decode_workspace_min_bytes > santa_noalloc_scratch_bytes(),
+ *     or more than (scratch - 256) / 4 (sequence, KV head) units (their arrival counters).
+ *     Every other argument error returns santa_decode's status; a refused call leaves the
+ *     array untouched.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *     with that device current and keeps it for the process; make that first call before any
+ *     stream capture.  The kept address is void after cudaDeviceReset on that device (the
+ *     module is then loaded again, possibly elsewhere): do not call this entry point after
+ *     a reset.
  *   - Every call on a device shares the one array, which keeps the previous call's
- *     contents; each call first clears the arrival counters in it (cudaMemsetAsync on the
- *     call's stream, no allocation).  Calls whose work overlaps on the GPU (different
- *     streams, or other threads) race on the array: serialise them.
+ *     contents.  When the plan spreads a unit over several clusters, the call first clears
+ *     the arrival counters at the array's start (cudaMemsetAsync on the call's stream, no
+ *     allocation).  Calls whose work overlaps on the GPU (different streams, or other
+ *     threads) race on the array: serialise them.
  */
 int santa_decode_noalloc(const santa_decode_args* a, void* stream);
 

@@ -526,11 +526,10 @@ def santa_decode(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int, 
 
 
 def santa_decode_noalloc(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws: int,
-                         seed: int, bufs: DecodeBuffers, team_probs: bool = False,
-                         stream=None) -> DecodeBuffers:
+                         seed: int, bufs: DecodeBuffers, stream=None) -> DecodeBuffers:
     """santa_decode with the library's built-in scratch instead of bufs.workspace, for
     callers that cannot allocate device memory at call time (the caller still provides the
-    outputs in bufs; bufs.workspace is not used)."""
+    outputs in bufs, team_probs included if wanted; bufs.workspace is not used)."""
     a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, seed, bufs)
     _check(lib().santa_decode_noalloc(ctypes.byref(a), _stream(stream)), "santa_decode_noalloc")
     return bufs

@@ -128,4 +128,9 @@ cudaError_t decode_launch_bf16_wide(const DecodeParams& p, int head_dim, int gro
 int decode_resident_bf16_wide(int head_dim, int group);
 int decode_max_clusters_bf16_wide(int head_dim, int group, int cluster);
 
+// Every host-side check santa_decode makes on `a`, then its launch plan; launches nothing
+// and touches no device memory.  On SANTA_OK *clusters_per_unit receives the plan's NC (> 1:
+// the partials and arrival counters go through a->workspace).
+int check_and_plan_decode(const santa_decode_args* a, int* clusters_per_unit);
+
 }  // namespace santa

@@ -294,7 +294,8 @@ int encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int d) {
   return r == CUDA_SUCCESS ? SANTA_OK : SANTA_ERR_CUDA;
 }
 
-int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
+// Every host-side check of a call in `mode`, then its plan; launches nothing.
+int check_and_plan(const santa_decode_args* a, int mode, Plan* pl) {
   int rc = check_inputs(a);
   if (rc) return rc;
   const bool sampling = mode == santa::kModeDecode || mode == santa::kModeSample;
@@ -306,16 +307,23 @@ int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   }
   if (mode != santa::kModeSample && (!a->out || !aligned(a->out, 16)))
     return SANTA_ERR_INVALID_ARG;
-  Plan pl;
-  if ((rc = make_plan(a, mode, &pl))) return rc;
+  if ((rc = make_plan(a, mode, pl))) return rc;
   const bool variant = a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f;
   if (sampling && variant) {
     // the variants are implemented where a CTA samples its whole unit in shared memory
     const int G = a->num_q_heads / a->num_kv_heads;
-    const int64_t per = ceil_div(a->max_teams, pl.cluster);
+    const int64_t per = ceil_div(a->max_teams, pl->cluster);
     if (a->max_teams > santa::kMaxTeamsPerCta || (G + 1) * per > santa::kPubScores)
       return SANTA_ERR_UNSUPPORTED;
   }
+  return SANTA_OK;
+}
+
+int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
+  Plan pl;
+  int rc = check_and_plan(a, mode, &pl);
+  if (rc) return rc;
+  const bool sampling = mode == santa::kModeDecode || mode == santa::kModeSample;
   DecodeParams p = {};
   p.q = a->q;
   p.k_pool = a->k_pool;
@@ -391,6 +399,15 @@ int do_reps(const void* k_pool, int dtype, int64_t num_pages, int hkv, int T, in
 }
 
 }  // namespace
+
+namespace santa {
+int check_and_plan_decode(const santa_decode_args* a, int* clusters_per_unit) {
+  Plan pl;
+  const int rc = check_and_plan(a, kModeDecode, &pl);
+  if (rc == SANTA_OK && clusters_per_unit) *clusters_per_unit = pl.clusters;
+  return rc;
+}
+}  // namespace santa
 
 // Only the C ABI is exported (the library is built with -fvisibility=hidden).
 #pragma GCC visibility push(default)

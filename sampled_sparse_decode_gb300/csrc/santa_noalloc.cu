@@ -45,25 +45,33 @@ void* scratch_address() {
 #pragma GCC visibility push(default)
 extern "C" int santa_decode_noalloc(const santa_decode_args* a, void* stream) {
   if (!a) return SANTA_ERR_INVALID_ARG;
+  // 1. Size checks, before any CUDA call: the shape's minimum split scratch, and the arrival
+  //    counters (one 32-bit word per unit, padded to 256 bytes), must both fit the array.
   const size_t need = santa_decode_workspace_min_bytes(a->batch, a->num_q_heads,
                                                        a->num_kv_heads, a->head_dim,
                                                        a->team_size, a->max_teams,
                                                        a->num_draws);
   if (need == 0) return SANTA_ERR_UNSUPPORTED;
-  if (need > kStaticScratchBytes) return SANTA_ERR_SCRATCH_LIMIT;
-  void* scratch = scratch_address();
-  if (!scratch) return SANTA_ERR_CUDA;
-  // The array keeps the previous call's contents.  Partials are always written before they
-  // are read, but the arrival counters at its start (one 32-bit word per unit, padded to
-  // 256 bytes; the array is 256-byte aligned, so the split plan puts them at offset 0) must
-  // start at zero: clear them on the call's stream.
   const size_t units = static_cast<size_t>(a->batch) * static_cast<size_t>(a->num_kv_heads);
   const size_t counters = (units * sizeof(uint32_t) + 255) / 256 * 256;
-  if (cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return SANTA_ERR_CUDA;
+  if (need > kStaticScratchBytes || counters + 256 > kStaticScratchBytes)
+    return SANTA_ERR_SCRATCH_LIMIT;
+  void* scratch = scratch_address();
+  if (!scratch) return SANTA_ERR_CUDA;
   santa_decode_args b = *a;
   b.workspace = scratch;
   b.workspace_bytes = kStaticScratchBytes;
+  // 2. Every argument check and the launch plan, still without touching the array.
+  int clusters = 1;
+  const int rc = santa::check_and_plan_decode(&b, &clusters);
+  if (rc != SANTA_OK) return rc;
+  // 3. The array keeps the previous call's contents.  Partials are always written before
+  //    they are read; the arrival counters (at the array's start: it is 256-byte aligned,
+  //    so the plan puts them at offset 0) are used only when several clusters share a unit,
+  //    and must then start at zero.  Clear them on the call's stream.
+  if (clusters > 1 &&
+      cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SANTA_ERR_CUDA;
   return santa_decode(&b, stream);
 }
 

@@ -194,3 +194,18 @@ def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
     a = valid_args()
     a.batch, a.num_q_heads, a.num_kv_heads, a.max_teams, a.num_draws = 64, 64, 8, 16384, 4096
     assert f(ctypes.byref(a), None) == SCRATCH_LIMIT
+    # one cluster per unit (M = 1), so the split partials need nothing, but 65535 x 32
+    # units' arrival counters (8 MiB) would not fit: refused before any CUDA call
+    a = valid_args()
+    a.batch, a.num_q_heads, a.num_kv_heads, a.num_draws = 65535, 32, 32, 1
+    assert f(ctypes.byref(a), None) == SCRATCH_LIMIT
+    # the largest unit count whose counters still fit passes the size checks (the call then
+    # fails on something else: no device here, or, on a GPU, the misaligned query, which is
+    # refused before the array is touched)
+    units_max = ((4 << 20) - 256) // 4
+    a = valid_args()
+    a.batch, a.num_q_heads, a.num_kv_heads, a.num_draws = units_max // 16, 16, 16, 1
+    lib.santa_decode_workspace_min_bytes.restype = ctypes.c_size_t
+    assert lib.santa_decode_workspace_min_bytes(a.batch, 16, 16, 128, 128, 256, 1) <= 4 << 20
+    a.q = 0x10008
+    assert f(ctypes.byref(a), None) != SCRATCH_LIMIT
