@@ -2,7 +2,7 @@
 """SANTA++ decode-step attention benchmark on GB300 — prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--cpu-seconds S] [--no-e2e]
+                    [--workload NAME] [--cpu-seconds S] [--no-e2e] [--no-extra]
 
 Workload: the Qwen2.5-7B-shaped decode attention layer at 32K context (1 sequence, 28 query
 / 4 KV heads, d = 128, T = 128, M = 31 draws, bf16 K/V, mixture keys), seeded synthetic
@@ -20,12 +20,18 @@ e2e        the same steps through the C ABI with pinned host buffers: per step o
            (StepInputs), runs the decode, copies out, draw/sampled ids, pi, |S| and the
            status word back device->host (packed DecodeBuffers) and waits for the stream.
 dense      the in-run dense split-K decode kernel on the same buffers (speed reference).
+workloads  the other full-size workloads (Qwen B=8 M=64, Llama paged B=16, 128K B=4) timed
+           the same way, each with its roofline fraction and dense kernel, and the 128K
+           workload's sweep over M in {16, 31, 64, 128}.
+timing     every entry point's K steps are replayed from CUDA graphs (each graph replayed
+           once before timing) behind a spin kernel, so the events time the device only.
 cpu_baseline  the fp64 C oracle, single-threaded, on a bounded sample of steps.
 --impl reference  times that oracle alone (the reference arm of this benchmark).
 """
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -57,6 +63,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time the headline workload only (not the other full-size ones)")
     ap.add_argument("--mode", choices=["bench", "profile", "accuracy", "loop"], default="bench",
                     help="profile: W + K plain santa_decode (or --dense) steps on one copy of "
                          "the inputs, for ncu captures; accuracy: error of every sampler "
@@ -74,6 +82,13 @@ def parse():
                     help="loop mode: tokens generated after the workload's context")
     ap.add_argument("--refresh", default="16,64,256",
                     help="loop mode: hold periods R of the sampled set (comma separated)")
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="write the per-launch DRAM traffic of the decode kernel, read from an "
+                         "ncu --csv log of dram__bytes_read.sum and dram__bytes_write.sum "
+                         "(bytes), to --traffic-out with the hash of the current kernel "
+                         "sources, and exit")
+    ap.add_argument("--traffic-out", default=None, help="where --record-traffic writes")
+    ap.add_argument("--traffic-command", default="", help="the ncu command, for the record")
     return ap.parse_args()
 
 
@@ -107,6 +122,34 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def host_cores():
+    """The host's logical cores and the cores this process may run on."""
+    try:
+        allowed = sorted(os.sched_getaffinity(0))
+    except AttributeError:
+        allowed = list(range(os.cpu_count() or 1))
+    return {"host_cores": os.cpu_count(), "affinity_cores": len(allowed),
+            "affinity": _ranges(allowed)}
+
+
+def _ranges(cores):
+    """[0, 1, 2, 5] -> "0-2,5"."""
+    out, i = [], 0
+    while i < len(cores):
+        j = i
+        while j + 1 < len(cores) and cores[j + 1] == cores[j] + 1:
+            j += 1
+        out.append(f"{cores[i]}-{cores[j]}" if j > i else f"{cores[i]}")
+        i = j + 1
+    return ",".join(out)
+
+
+def host_cores_note():
+    h = host_cores()
+    return (f"1 thread on a host of {h['host_cores']} cores "
+            f"(affinity mask: {h['affinity_cores']} cores, {h['affinity']})")
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -126,6 +169,52 @@ def recorded_traffic(workload):
     except Exception:
         pass
     return None
+
+
+_BYTE_UNITS = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12}
+
+
+def parse_ncu_traffic(csv_path, kernel_regex="decode_kernel"):
+    """Per captured launch of the matching kernel (in launch order): (name, DRAM bytes read,
+    DRAM bytes written), from an `ncu --csv` log with one row per metric."""
+    import csv
+    import re
+    launches = {}
+    with open(csv_path, newline="") as f:
+        lines = [l for l in f if l.startswith('"')]       # drop ncu's own log lines
+    for row in csv.DictReader(lines):
+        name = row.get("Kernel Name", "")
+        metric = row.get("Metric Name", "")
+        if not re.search(kernel_regex, name) or metric not in ("dram__bytes_read.sum",
+                                                                "dram__bytes_write.sum"):
+            continue
+        unit = _BYTE_UNITS[row.get("Metric Unit", "byte").strip().lower()]
+        val = float(row["Metric Value"].replace(",", "")) * unit
+        rec = launches.setdefault(int(row["ID"]), {"name": name})
+        rec["read" if metric.endswith("read.sum") else "write"] = val
+    return [(r["name"], r["read"], r["write"]) for _, r in sorted(launches.items())
+            if "read" in r and "write" in r]
+
+
+def record_traffic_file(csv_path, out_path, workload, command):
+    """The committed traffic record: mean DRAM bytes per decode launch, keyed by the hash of
+    the kernel sources this script sees, so the bench uses it only for those sources."""
+    launches = parse_ncu_traffic(csv_path)
+    if not launches:
+        raise SystemExit(f"no decode_kernel launches with DRAM metrics in {csv_path}")
+    rd = [r for _, r, _ in launches]
+    wr = [w for _, _, w in launches]
+    rec = {"kernel": launches[0][0], "workload": workload,
+           "kernel_source_sha": kernel_source_sha(),
+           "dram_bytes_per_launch": (sum(rd) + sum(wr)) / len(launches),
+           "dram_bytes_read_per_launch": rd, "dram_bytes_write_per_launch": wr,
+           "command": command,
+           "note": "cold caches (ncu flushes them before each launch); written by "
+                   "bench.py --record-traffic from the ncu log"}
+    with open(out_path, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
 
 
 class ClockSampler:
@@ -249,25 +338,239 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
-                   "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "seq_len": cfg.seq_len,
-                   "team_size": cfg.team_size, "draws": cfg.draws},
+        "config": config_of(cfg, world),
         "sampler": {"name": smp, "mix_alpha": alpha},
         "cpu_baseline": {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": f"{sample}; {host_cores_note()}", **host_cores()},
         "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
 
 # ---------------------------------------------------------------------------- GPU arm
 
+# Full-size workloads timed beside the headline one, each the same way, and the draw counts
+# of the long-context sweep (against the same dense kernel).
+EXTRA_WORKLOADS = ("qwen7b_32k_b8_m64", "llama8b_paged_32k_b16_m32", "long_128k_b4_m64")
+SWEEP_WORKLOAD = "long_128k_b4_m64"
+SWEEP_DRAWS = (16, 31, 64, 128)
+SPIN_CYCLES = 400_000          # ~0.2 ms at 2 GHz: the host enqueues the timed graphs meanwhile
+
+
+def config_of(cfg, world):
+    """The workload description shared by both arms of the bench line."""
+    return {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
+            "kv_heads": cfg.kv_heads, "head_dim": cfg.head_dim, "seq_len": cfg.seq_len,
+            "team_size": cfg.team_size, "draws": cfg.draws,
+            "parallelism": "replicas" if world > 1 else "1gpu",
+            "l2": "inputs larger than L2: K, V and the representatives rotate over copies, "
+                  ">= 6x the L2 size touched between two uses of a copy",
+            "timing": "CUDA graphs of whole steps, every graph replayed once before timing, "
+                      "CUDA events on the launching stream behind a spin kernel"}
+
+
+def _dev_tensor(a, dev):
+    import numpy as np
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(a).to(dev)
+
+
+class Rig:
+    """One workload resident in HBM: R rotating copies of K, V and the representatives, so
+    that the bytes the decode touches between two uses of a copy, (R - 1) steps' worth at
+    |S| = M for the smallest M timed on it, exceed 6x the L2 size."""
+
+    def __init__(self, name, dev, draws=None, min_draws=None):
+        import torch
+        import sampled_sparse_decode_gb300 as santa
+        from sampled_sparse_decode_gb300 import workloads as W
+        wl = W.generate(name, **({"draws": draws} if draws else {}))
+        cfg = wl.cfg
+        self.wl, self.cfg, self.dev = wl, cfg, dev
+        self.esize = 2 if cfg.dtype == "bf16" else 4
+        self.units = cfg.batch * cfg.kv_heads
+        self.n_teams = wl.max_teams
+        d, T = cfg.head_dim, cfg.team_size
+        self.q = _dev_tensor(wl.q, dev)
+        self.pt, self.lens, self.fill = (_dev_tensor(x, dev) for x in
+                                         (wl.page_table, wl.seq_lens, wl.page_fill))
+        k0, v0 = _dev_tensor(wl.k_pool, dev), _dev_tensor(wl.v_pool, dev)
+        reps0 = santa.santa_build_reps(k0, self.fill)
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        m_small = min(cfg.draws, min_draws or cfg.draws, self.n_teams)
+        self.touched = self.units * (self.n_teams * d * 4 + m_small * T * 2 * d * self.esize)
+        pool = 2 * k0.numel() * self.esize + reps0.numel() * 4
+        free, _ = torch.cuda.mem_get_info(dev)
+        R = 1 + math.ceil(6 * self.l2 / self.touched)
+        self.R = max(2, min(R, int(0.4 * free // pool)))
+        self.ks = [k0] + [k0.clone() for _ in range(self.R - 1)]
+        self.vs = [v0] + [v0.clone() for _ in range(self.R - 1)]
+        self.reps = [reps0] + [reps0.clone() for _ in range(self.R - 1)]
+        self.dense_kv = self.units * cfg.seq_len * 2 * d * self.esize
+
+    def bufs(self, M, dense=False, team_probs=False):
+        from sampled_sparse_decode_gb300 import binding as Bn
+        c = self.cfg
+        return Bn.DecodeBuffers.allocate(self.q.dtype, c.batch, c.q_heads, c.kv_heads,
+                                         c.head_dim, c.team_size, self.n_teams, M, self.dev,
+                                         dense=dense, team_probs=team_probs)
+
+    def args(self, M, bufs, sampler="iid_ht", alpha=0.0, dense=False):
+        """One argument structure per rotation copy; rotation r decodes with seed r."""
+        from sampled_sparse_decode_gb300 import binding as Bn
+        return [Bn._args(self.q, self.ks[r], self.vs[r], None if dense else self.reps[r],
+                         self.pt, self.lens, 1 if dense else M, 0 if dense else r, bufs,
+                         sampler, alpha) for r in range(self.R)]
+
+    def step_bytes(self, mean_sel):
+        """Algorithmic bytes of one decode step at the realised mean |S|: the representatives
+        of every team, K and V of the sampled teams, q and out."""
+        c = self.cfg
+        d, T = c.head_dim, c.team_size
+        return (self.units * self.n_teams * d * 4 + mean_sel * self.units * T * 2 * d * self.esize
+                + c.batch * c.q_heads * d * (self.esize + 4))
+
+    def sampled(self, M, a_list, bufs, lib, stream, call):
+        """Mean |S| over the R seeds the graphs replay, and the share of teams whose sampling
+        probability p_i (and inclusion probability pi_i) is below 1%, from seed 0."""
+        import torch
+        sel_total = 0
+        with torch.cuda.stream(stream):
+            for r in range(self.R):
+                call(lib.santa_sample, a_list[r])
+                stream.synchronize()
+                sel_total += int(bufs.sel_count.sum().item())
+        assert int(bufs.device_status.item()) == 0
+        mean_sel = sel_total / (self.R * self.units)
+        tp = self.bufs(M, team_probs=True)
+        a0 = self.args(M, tp)[0]
+        with torch.cuda.stream(stream):
+            call(lib.santa_sample, a0)
+        stream.synchronize()
+        assert int(tp.device_status.item()) == 0
+        p = tp.team_probs.double()
+        n_valid = torch.div(self.lens.long() + self.cfg.team_size - 1, self.cfg.team_size,
+                            rounding_mode="floor")
+        valid = (torch.arange(self.n_teams, device=p.device)[None, None, :] <
+                 n_valid[:, None, None]).expand_as(p)
+        pi = -torch.expm1(M * torch.log1p(-p.clamp(max=1.0)))
+        nv = float(valid.sum()) or 1.0
+        rejected = {"p_below_1pct": float(((p < 0.01) & valid).sum()) / nv,
+                    "pi_below_1pct": float(((pi < 0.01) & valid).sum()) / nv,
+                    "teams": int(nv), "seed": 0}
+        return mean_sel, rejected
+
+
+class Timer:
+    """Exactly K steps of one entry point, replayed from CUDA graphs over a rig's rotation
+    copies: K // R replays of an R-step graph and one (K mod R)-step tail.  Every graph is
+    replayed once untimed (the tail first, so the last warm-up replay is the full graph and
+    every copy's reuse is R - 1 steps apart), at least W steps in all.  The timed replays are
+    enqueued behind a spin kernel, so the events time the device, not the host's launches."""
+
+    def __init__(self, dev, stream, world):
+        self.dev, self.stream, self.world = dev, stream, world
+
+    def call(self, fn, a):
+        rc = fn(ctypes.byref(a), self.stream.cuda_stream)
+        if rc:
+            raise RuntimeError(f"{fn.__name__}: status {rc}")
+
+    def capture(self, body):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.stream):
+            body()                                   # attribute set-up, lazy loading
+            self.stream.synchronize()
+            with torch.cuda.graph(g, stream=self.stream):
+                body()
+        return g
+
+    def barrier(self):
+        import torch
+        if self.world > 1:
+            torch.distributed.barrier()
+
+    def run(self, make, R, K, W_, label):
+        """make(n) -> a graph of n steps over rotations 0..n-1.  Returns (device seconds for
+        the K steps, (wall start, wall end))."""
+        import torch
+        full, tail = divmod(K, R)
+        g_full = make(R)
+        g_tail = make(tail) if tail else None
+        with torch.cuda.stream(self.stream):
+            if g_tail is not None:
+                g_tail.replay()
+            for _ in range(max(1, math.ceil(W_ / R))):
+                g_full.replay()
+        torch.cuda.synchronize(self.dev)
+        self.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push(label)
+        t0 = time.time()
+        with torch.cuda.stream(self.stream):
+            torch.cuda._sleep(SPIN_CYCLES)
+            e0.record(self.stream)
+            for _ in range(full):
+                g_full.replay()
+            if g_tail is not None:
+                g_tail.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        t1 = time.time()
+        torch.cuda.nvtx.range_pop()
+        self.barrier()
+        return e0.elapsed_time(e1) / 1e3, (t0, t1)
+
+    def steps(self, fn, a_list, K, W_, label):
+        """Seconds per step of `fn` (an entry point taking a santa_decode_args) over a_list."""
+        make = lambda n: self.capture(lambda: [self.call(fn, a_list[r]) for r in range(n)])
+        sec, window = self.run(make, len(a_list), K, W_, label)
+        return sec / K, window
+
+
+def measure_workload(rig, timer, lib, K, W_, peak, draws=None, dense_s=None, sampler="iid_ht",
+                     alpha=0.0):
+    """Decode, sampling-only and dense steps of one rig, each K steps timed the same way."""
+    from sampled_sparse_decode_gb300 import binding as Bn
+    cfg = rig.cfg
+    M = draws or cfg.draws
+    bufs = rig.bufs(M)
+    a_dec = rig.args(M, bufs, sampler, alpha)
+    tag = f"{cfg.name} M={M}"
+    step_s, window = timer.steps(lib.santa_decode, a_dec, K, W_, f"decode {tag}")
+    smp_s, _ = timer.steps(lib.santa_sample, a_dec, K, W_, f"sample {tag}")
+    mean_sel, rejected = rig.sampled(M, a_dec, bufs, lib, timer.stream, timer.call)
+    if dense_s is None:
+        dbufs = rig.bufs(1, dense=True)
+        dense_s, _ = timer.steps(lib.santa_dense_decode, rig.args(1, dbufs, dense=True), K, W_,
+                                 f"dense {cfg.name}")
+    sbytes = rig.step_bytes(mean_sel)
+    plan = Bn.santa_decode_plan(rig.q, rig.ks[0], rig.pt, M)
+    dplan = Bn.santa_decode_plan(rig.q, rig.ks[0], rig.pt, 1, which="dense")
+    res = {
+        "draws": M, "step_us": step_s * 1e6, "steps_per_s": 1.0 / step_s,
+        "bytes_per_step": sbytes, "hbm_gbs": sbytes / step_s / 1e9,
+        "frac": sbytes / step_s / 1e9 / peak, "mean_sel": mean_sel,
+        "kv_read_ratio": mean_sel * rig.units * cfg.team_size * 2 * cfg.head_dim * rig.esize /
+                         rig.dense_kv,
+        "sample_only_us": smp_s * 1e6,
+        "dense_us": dense_s * 1e6, "dense_hbm_gbs": rig.dense_kv / dense_s / 1e9,
+        "dense_frac": rig.dense_kv / dense_s / 1e9 / peak,
+        "speedup_vs_dense": dense_s / step_s,
+        "rejected_teams": rejected,
+        "plan": {"decode": plan, "dense": dplan}, "rotations": rig.R, "steps": K,
+    }
+    return res, window, dense_s
+
+
 def run_ours(args):
     import numpy as np
     import torch
     import sampled_sparse_decode_gb300 as santa
     from sampled_sparse_decode_gb300 import binding as Bn
-    from sampled_sparse_decode_gb300 import workloads as W
-    import ctypes
 
     world, rank, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -276,163 +579,65 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
-    wl = W.generate(args.workload, **({'draws': args.draws} if args.draws else {}))
-    cfg = wl.cfg
     lib = Bn.lib()
-    esize = 2 if cfg.dtype == "bf16" else 4
-    units = cfg.batch * cfg.kv_heads
-    G, d, T, M = cfg.group, cfg.head_dim, cfg.team_size, cfg.draws
-    n_teams = wl.max_teams
-
-    def t(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    q, k0, v0 = t(wl.q), t(wl.k_pool), t(wl.v_pool)
-    pt, lens, fill = t(wl.page_table), t(wl.seq_lens), t(wl.page_fill)
-    reps0 = santa.santa_build_reps(k0, fill)
-
-    # rotation: bytes touched per step (upper bound, |S| = M) x R >= 6 x L2
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    touched = units * (n_teams * d * 4 + min(M, n_teams) * T * 2 * d * esize)
-    pool_bytes = 2 * k0.numel() * esize + reps0.numel() * 4
-    free, _ = torch.cuda.mem_get_info(dev)
-    R = max(2, math.ceil(6 * l2 / touched))
-    R = min(R, max(2, int(0.4 * free // pool_bytes)))
-    ks = [k0] + [k0.clone() for _ in range(R - 1)]
-    vs = [v0] + [v0.clone() for _ in range(R - 1)]
-    reps = [reps0] + [reps0.clone() for _ in range(R - 1)]
-    bufs = Bn.DecodeBuffers.allocate(q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads, d, T,
-                                     n_teams, M, dev)
-    dbufs = Bn.DecodeBuffers.allocate(q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads, d, T,
-                                      n_teams, M, dev, dense=True)
-    args_r = [Bn._args(q, ks[r], vs[r], reps[r], pt, lens, M, r, bufs, args.sampler,
-                       args.mix_alpha) for r in range(R)]
-    dargs_r = [Bn._args(q, ks[r], vs[r], None, pt, lens, 1, 0, dbufs) for r in range(R)]
     stream = torch.cuda.Stream(device=dev)
-    sh = stream.cuda_stream
-
-    def call(fn, a):
-        rc = fn(ctypes.byref(a), sh)
-        if rc:
-            raise RuntimeError(f"{fn.__name__}: status {rc}")
-
-    def capture(body):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            body()                                   # warm (attribute set-up, lazy loading)
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                body()
-        return g
-
-    def rounds(fn, arg_list):
-        """Graph maker for n steps of `fn` over the rotations (n <= R)."""
-        def make(nsteps):
-            return capture(lambda: [call(fn, arg_list[r]) for r in range(nsteps)])
-        return make
-
-    def timed(make, K, W_):
-        """Exactly K steps: K // R replays of an R-step graph and one (K mod R)-step tail."""
-        full, tail = K // R, K % R
-        g_full = make(R)
-        g_tail = make(tail) if tail else None
-        with torch.cuda.stream(stream):
-            for _ in range(max(1, math.ceil(W_ / R))):
-                g_full.replay()
-        torch.cuda.synchronize(dev)
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0 = time.time()
-        e0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(full):
-                g_full.replay()
-            if g_tail is not None:
-                g_tail.replay()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        t1 = time.time()
-        barrier()
-        return e0.elapsed_time(e1) / 1e3, K, (t0, t1)
-
+    timer = Timer(dev, stream, world)
     K, W_ = args.steps, max(3, args.warmup)
+    peak, peak_kind = measured_peak()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
 
-    # ---- headline: whole decode steps
-    sec, steps_done, (c0, c1) = timed(rounds(lib.santa_decode, args_r), K, W_)
-    value, sec = job_rate(sec, steps_done, world, dev)
-    step_s = sec / steps_done
-
-    # realised |S| of the R seeds (the graph replays them)
-    sel_total = 0
-    with torch.cuda.stream(stream):
-        for r in range(R):
-            call(lib.santa_sample, args_r[r])
-            stream.synchronize()
-            sel_total += int(bufs.sel_count.sum().item())
-    mean_sel = sel_total / (R * units)
-    assert int(bufs.device_status.item()) == 0
-
-    # ---- the two halves alone, for the breakdown: sampling only, attention only (on the
-    # sampled sets of the last seed)
-    sec_s, n_s, _ = timed(rounds(lib.santa_sample, args_r), K, W_)
-    smp_s = sec_s / n_s
-    sec_a, n_a, _ = timed(rounds(lib.santa_attend, args_r), K, W_)
-    att_s = sec_a / n_a
-
-    # ---- dense split-K reference on the same buffers
-    sec_d, n_d, _ = timed(rounds(lib.santa_dense_decode, dargs_r), max(R, K // 4), W_)
-    dense_s = sec_d / n_d
-    clocks.stop()
-    clk = clocks.summary(c0, c1)
-
-    # ---- algorithmic bytes per step (realised |S|): the representatives of every team, K
-    # and V of the sampled teams, q and out.  One launch of the fused kernel per step.
-    step_bytes = (units * n_teams * d * 4 + mean_sel * units * T * 2 * d * esize +
-                  cfg.batch * cfg.q_heads * d * (esize + 4))
-    dense_kv = units * cfg.seq_len * 2 * d * esize
-    peak, peak_kind = measured_peak()
+    # ---- headline workload: whole decode steps, the two halves alone, and the dense kernel
+    rig = Rig(args.workload, dev, draws=args.draws)
+    cfg = rig.cfg
+    G, d, T, M = cfg.group, cfg.head_dim, cfg.team_size, cfg.draws
+    units, n_teams = rig.units, rig.n_teams
+    head, (c0, c1), dense_s = measure_workload(rig, timer, lib, K, W_, peak,
+                                               sampler=args.sampler, alpha=args.mix_alpha)
+    step_s = head["step_us"] / 1e6
+    value, slowest = job_rate(step_s * K, K, world, dev)
+    step_s = slowest / K
+    bufs = rig.bufs(M)
+    a_dec = rig.args(M, bufs, args.sampler, args.mix_alpha)
+    att_s, _ = timer.steps(lib.santa_attend, a_dec, K, W_, "attend")  # sets of the last seed
+    step_bytes = rig.step_bytes(head["mean_sel"])
     achieved = step_bytes / step_s / 1e9
 
     # ---- the step before the decode: one appended token per unit (santa_append_kv) at the
-    # last slot of every sequence, replayed from a CUDA graph of R calls
+    # last slot of every sequence
+    q = rig.q
     kn = torch.randn((cfg.batch, cfg.kv_heads, d), device=dev).to(q.dtype)
     vn = torch.randn((cfg.batch, cfg.kv_heads, d), device=dev).to(q.dtype)
-    last = (lens - 1).contiguous()
-    nxt = torch.empty_like(lens)
+    last = (rig.lens - 1).contiguous()
+    nxt = torch.empty_like(rig.lens)
 
-    def append_call(r):
-        santa.santa_append_kv(kn, vn, ks[r], vs[r], reps[r], pt, last, nxt, stream=stream)
+    def append_make(n):
+        return timer.capture(lambda: [santa.santa_append_kv(kn, vn, rig.ks[r], rig.vs[r],
+                                                            rig.reps[r], rig.pt, last, nxt,
+                                                            stream=stream) for r in range(n)])
 
-    def append_make(nsteps):
-        return capture(lambda: [append_call(r) for r in range(nsteps)])
-
-    sec_app, n_app, _ = timed(append_make, max(R, min(K, 1000)), W_)
+    n_app = max(rig.R, min(K, 1000))
+    sec_app, _ = timer.run(append_make, rig.R, n_app, W_, "append")
     append_us = sec_app / n_app * 1e6
 
     # ---- the representatives of the whole cache (santa_build_reps, once after prefill): a
     # rebuild of every rotation copy in place from its own keys (the same values again)
-    def reps_make(nsteps):
-        return capture(lambda: [santa.santa_build_reps(ks[r], fill, reps=reps[r], stream=stream)
-                                for r in range(nsteps)])
+    def reps_make(n):
+        return timer.capture(lambda: [santa.santa_build_reps(rig.ks[r], rig.fill,
+                                                             reps=rig.reps[r], stream=stream)
+                                      for r in range(n)])
 
-    sec_rep, n_rep, _ = timed(reps_make, max(R, min(K, 200)), W_)
+    n_rep = max(rig.R, min(K, 200))
+    sec_rep, _ = timer.run(reps_make, rig.R, n_rep, W_, "build_reps")
     reps_us = sec_rep / n_rep * 1e6
-    valid_tokens = int(wl.page_fill.astype(np.int64).sum())
-    reps_bytes = valid_tokens * cfg.kv_heads * d * esize + reps0.numel() * 4
+    valid_tokens = int(rig.wl.page_fill.astype(np.int64).sum())
+    reps_bytes = valid_tokens * cfg.kv_heads * d * rig.esize + rig.reps[0].numel() * 4
 
     # ---- accuracy proxy: relative L2 error of the estimate against dense attention, per
     # query head, over 32 seeds (no model or dataset here: retention cannot be measured)
-    acc = accuracy_vs_dense(q, ks[0], vs[0], reps[0], pt, lens, M, args.sampler, args.mix_alpha,
-                            32, santa)
+    acc = accuracy_vs_dense(q, rig.ks[0], rig.vs[0], rig.reps[0], rig.pt, rig.lens, M,
+                            args.sampler, args.mix_alpha, 32, santa)
 
     # ---- end to end through the Python API, host buffers: per step one call of
     # santa_decode_host (PreparedDecode.run_host over the rotation's buffers): one
@@ -442,64 +647,99 @@ def run_ours(args):
     if not args.no_e2e:
         inp = santa.StepInputs.allocate(q.dtype, cfg.batch, cfg.q_heads, d, n_teams, dev)
         inp.host_q.copy_(q.cpu())
-        inp.host_page_table.copy_(pt.cpu())
-        inp.host_seq_lens.copy_(lens.cpu())
+        inp.host_page_table.copy_(rig.pt.cpu())
+        inp.host_seq_lens.copy_(rig.lens.cpu())
         pbufs = santa.DecodeBuffers.allocate(q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads, d,
                                              T, n_teams, M, dev, packed=True)
         host = pbufs.host_mirror()
-        preps = [santa.santa_decode_prepared(inp.q, ks[r], vs[r], reps[r], inp.page_table,
-                                             inp.seq_lens, M, bufs=pbufs, sampler=args.sampler,
-                                             mix_alpha=args.mix_alpha) for r in range(R)]
+        preps = [santa.santa_decode_prepared(inp.q, rig.ks[r], rig.vs[r], rig.reps[r],
+                                             inp.page_table, inp.seq_lens, M, bufs=pbufs,
+                                             sampler=args.sampler, mix_alpha=args.mix_alpha)
+                 for r in range(rig.R)]
         h2d = inp.host_slab.numel()
         d2h = host.slab.numel()
         K_e = max(20, min(K, 2000))
 
         def e2e_step(s):
-            preps[s % R].run_host(s, inp, host, stream)
+            preps[s % rig.R].run_host(s, inp, host, stream)
 
         for s in range(W_):
             e2e_step(s)
-        barrier()
+        timer.barrier()
+        torch.cuda.nvtx.range_push("e2e")
         t0 = time.perf_counter()
         for s in range(K_e):
             e2e_step(W_ + s)
         el = time.perf_counter() - t0
+        torch.cuda.nvtx.range_pop()
         e2e_rate, el = job_rate(el, K_e, world, dev)
         assert int(host.device_status[0]) == 0
         e2e = {"value": e2e_rate, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": K_e}
+    head_rot = rig.R
+    del rig, bufs, a_dec
+    torch.cuda.empty_cache()
+
+    # ---- the other full-size workloads, each timed like the headline (its own rotation
+    # copies), and the long-context draw sweep against one dense measurement
+    workloads = {}
+    if not args.no_extra:
+        for name in EXTRA_WORKLOADS:
+            if name == cfg.name:
+                continue
+            sweep = name == SWEEP_WORKLOAD
+            r_ = Rig(name, dev, min_draws=min(SWEEP_DRAWS) if sweep else None)
+            res, _, d_s = measure_workload(r_, timer, lib, K, W_, peak)
+            workloads[name] = res
+            if sweep:
+                rows = []
+                for m in SWEEP_DRAWS:
+                    row = res if m == r_.cfg.draws else \
+                        measure_workload(r_, timer, lib, K, W_, peak, draws=m, dense_s=d_s)[0]
+                    rows.append({k: row[k] for k in ("draws", "step_us", "bytes_per_step",
+                                                     "hbm_gbs", "frac", "mean_sel",
+                                                     "kv_read_ratio", "dense_us",
+                                                     "speedup_vs_dense")})
+                workloads[f"{name} draw sweep"] = rows
+            del r_
+            torch.cuda.empty_cache()
+    clocks.stop()
+    clk = clocks.summary(c0, c1)
+    clk_all = clocks.summary(0.0, float("inf"))
 
     # ---- CPU baseline (rank 0, single GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        from sampled_sparse_decode_gb300 import workloads as W
+        wl = W.generate(args.workload, **({'draws': args.draws} if args.draws else {}))
         v, n, el = oracle_steps_per_s(wl, args.cpu_seconds, sampler=args.sampler,
                                       alpha=args.mix_alpha)
         cpu = {"value": v, "unit": "steps/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} whole decode steps ({units} units each) in {el:.1f} s, "
-                         f"fp64 C oracle, one thread, reps precomputed"}
+                         f"fp64 C oracle, reps precomputed; {host_cores_note()}",
+               **host_cores()}
 
     if rank != 0:
         return
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
-        "steps": steps_done, "warmup": W_, "ms_per_step": step_s * 1e3,
+        "steps": K, "warmup": W_, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.q_heads,
-                   "kv_heads": cfg.kv_heads, "head_dim": d, "seq_len": cfg.seq_len,
-                   "team_size": T, "draws": M, "parallelism": "replicas" if world > 1 else "1gpu",
-                   "l2": f"inputs rotate over {R} copies of K/V/reps; touched bytes between "
-                         f"reuses of a copy >= 6x L2 at |S| = M ({l2 / 1e6:.0f} MB)",
-                   "timing": "CUDA graph of R steps replayed, CUDA events on the stream"},
+        "config": config_of(cfg, world),
+        "rotation": {"copies": head_rot, "bytes_touched_per_step": step_bytes,
+                     "l2_bytes": torch.cuda.get_device_properties(dev).L2_cache_size},
         "step_latency_us": step_s * 1e6,
-        "hbm_gbs_step": step_bytes / step_s / 1e9,
+        "hbm_gbs_step": achieved,
         "bytes_per_step": step_bytes,
-        "kv_read_ratio": mean_sel * units * T * 2 * d * esize / dense_kv,
-        "mean_sel": mean_sel,
+        "kv_read_ratio": head["kv_read_ratio"],
+        "mean_sel": head["mean_sel"],
         "dense": {"steps_per_s": 1.0 / dense_s, "latency_us": dense_s * 1e6,
-                  "hbm_gbs": dense_kv / dense_s / 1e9},
+                  "hbm_gbs": head["dense_hbm_gbs"], "frac": head["dense_frac"],
+                  "plan": head["plan"]["dense"]},
         "speedup_vs_dense": dense_s / step_s,
-        "kernels_us": {"decode": step_s * 1e6, "sample_only": smp_s * 1e6,
+        "kernels_us": {"decode": step_s * 1e6, "sample_only": head["sample_only_us"],
                        "attend_only": att_s * 1e6, "dense": dense_s * 1e6,
                        "append_token": append_us, "build_reps": reps_us},
         "build_reps": {"us": reps_us, "bytes": reps_bytes,
@@ -513,12 +753,16 @@ def run_ours(args):
                                "one launch per step",
                      "bytes_per_launch": step_bytes,
                      "traffic": recorded_traffic(cfg.name)},
+        "plan": head["plan"]["decode"],
+        "rejected_teams": head["rejected_teams"],
+        "workloads": workloads,
         "sampler": {"name": args.sampler, "mix_alpha": args.mix_alpha},
         "accuracy": acc,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": steps_done,
+        "gpu_launches": K,
         "clocks": clk,
+        "clocks_whole_run": clk_all,
     }
     print(json.dumps(line))
 
@@ -782,6 +1026,11 @@ def run_profile(args):
 
 def main():
     args = parse()
+    if args.record_traffic:
+        rec = record_traffic_file(args.record_traffic, args.traffic_out or TRAFFIC_FILE,
+                                  args.workload, args.traffic_command)
+        print(json.dumps(rec))
+        return
     if args.mode == "profile":
         run_profile(args)
     elif args.mode == "accuracy":

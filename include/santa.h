@@ -257,6 +257,16 @@ int santa_decode_plan(const santa_decode_args* a, int which, int32_t* out);
 int santa_decode(const santa_decode_args* a, void* stream);
 
 /*
+ * santa_decode_path — which form of the kernel santa_decode(a) runs (a's pointers need not
+ * be valid; shapes, sampler, mix_alpha and workspace_bytes are read).  1: the compact form,
+ * for bf16 steps with i.i.d. Horvitz-Thompson draws, no mixture, one cluster per unit and at
+ * most 1024 teams per sequence, whose sampling prologue is compiled without the general
+ * form's branches; 0: the general form; a negative santa_status for a refused shape.  Both
+ * forms compute the same step.
+ */
+int santa_decode_path(const santa_decode_args* a);
+
+/*
  * santa_dense_decode — exact dense softmax attention over all seq_len tokens of every
  * sequence, split-K over the paged cache (the speed reference the sampled path is compared
  * with; [ABS] compares against a dense FlashAttention baseline).  Reads q, k_pool, v_pool,

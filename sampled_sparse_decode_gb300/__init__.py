@@ -12,7 +12,7 @@ _BINDING_NAMES = (
     "santa_build_reps", "santa_update_reps", "santa_sample", "santa_attend", "santa_decode",
     "santa_dense_decode", "santa_decode_workspace_bytes", "santa_decode_workspace_min_bytes",
     "santa_dense_workspace_bytes", "santa_abi_version", "santa_status_string", "DecodeBuffers",
-    "santa_decode_noalloc", "santa_noalloc_scratch_bytes", "santa_decode_plan",
+    "santa_decode_noalloc", "santa_noalloc_scratch_bytes", "santa_decode_plan", "santa_decode_path",
     "SantaError", "DEV_BAD_PAGE", "DEV_BAD_SEQLEN", "DEV_BAD_SEL", "santa_append_kv", "SAMPLERS",
     "santa_attend_vs", "StepInputs", "HostOutputs", "PreparedDecode", "santa_decode_prepared",
 )

@@ -79,6 +79,7 @@ def lib():
             "santa_decode_noalloc": (i32, [A, vp]),
             "santa_decode_host": (i32, [A, vp, vp, sz, vp, vp, sz, vp]),
             "santa_decode_plan": (i32, [A, i32, vp]),
+            "santa_decode_path": (i32, [A]),
             "santa_noalloc_scratch_bytes": (sz, []),
         }
         for name, (res, args) in sigs.items():
@@ -561,6 +562,28 @@ def santa_decode_plan(q, k_pool, page_table, num_draws: int, which: str = "decod
     _check(lib().santa_decode_plan(ctypes.byref(a), _PLAN_MODES[which], out), "santa_decode_plan")
     return {"cluster": out[0], "clusters_per_unit": out[1], "teams_per_cta": out[2],
             "max_active_clusters": out[3], "wide": bool(out[4])}
+
+
+def santa_decode_path(q, k_pool, page_table, num_draws: int, sampler: str = "iid_ht",
+                      mix_alpha: float = 0.0, workspace_bytes: int | None = None) -> str:
+    """"compact" or "general": the form of the decode kernel santa_decode runs for these
+    shapes and sampler settings (with the default workspace unless workspace_bytes)."""
+    B, Hq, d = q.shape
+    _, Hkv, T, _ = k_pool.shape
+    a = _DecodeArgs()
+    a.dtype, a.batch, a.num_q_heads, a.num_kv_heads = _DTYPES[q.dtype], B, Hq, Hkv
+    a.head_dim, a.team_size, a.max_teams, a.num_draws = d, T, page_table.shape[1], num_draws
+    a.num_pages = k_pool.shape[0]
+    a.sampler, a.mix_alpha = SAMPLERS[sampler], float(mix_alpha)
+    if workspace_bytes is None:
+        workspace_bytes = santa_decode_workspace_bytes(q.dtype, B, Hq, Hkv, d, T,
+                                                       page_table.shape[1], num_draws)
+    a.workspace = 256 if workspace_bytes else None        # only its size is read
+    a.workspace_bytes = workspace_bytes
+    rc = lib().santa_decode_path(ctypes.byref(a))
+    if rc < 0:
+        _check(-rc, "santa_decode_path")
+    return "compact" if rc == 1 else "general"
 
 
 def santa_noalloc_scratch_bytes() -> int:

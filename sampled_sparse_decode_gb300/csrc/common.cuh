@@ -132,6 +132,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+// One contiguous bulk copy from this CTA's shared memory into another CTA's of the cluster
+// (TMA), completing `bytes` transaction bytes on the destination CTA's mbarrier; dst and
+// bar are cluster addresses (cluster_addr), src a local one.  All multiples of 16 bytes.
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Two-dimensional tensor copy global -> shared through a tensor map (TMA): the box at
 // (x, y) (x the innermost coordinate, in elements) lands at dst and completes on bar.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
@@ -243,6 +261,20 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
     const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
     const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
     c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+  }
+  return c;
+}
+
+// The same generator with its rounds in a loop: a tenth of the instructions, for code that
+// runs once per launch, where fetching the unrolled form costs more than the loop.
+__device__ __forceinline__ uint4 philox4x32_10_compact(uint4 c, uint2 k) {
+#pragma unroll 1
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    k.x += 0x9E3779B9u;
+    k.y += 0xBB67AE85u;
   }
   return c;
 }

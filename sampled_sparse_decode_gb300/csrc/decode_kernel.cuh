@@ -123,9 +123,52 @@ struct DecodeTraits {
   static constexpr size_t kPOff = kTableOff + sizeof(ChunkMeta) * kMaxChunksPerSplit;
   static constexpr size_t kAOff = kPOff + sizeof(float) * kWarps * 64;
   static constexpr size_t kBarOff = kAOff + sizeof(float) * kWarps * kMaxGroup;
-  static constexpr size_t kSmem = kBarOff + sizeof(uint64_t) * kStages;
+  // mbarriers: one per stage, then two of the compact path (staged rows, score exchange)
+  static constexpr size_t kSmem = kBarOff + sizeof(uint64_t) * (kStages + 2);
   static constexpr int kMinBlocks = (!W && kSmem <= 112 * 1024) ? 2 : 1;
   static_assert(!W || (BF16 && kStages % 2 == 0), "wide: bf16 only, even stage count");
+
+  // Compact path (a decode step with i.i.d. Horvitz-Thompson draws, no mixture, one cluster
+  // per unit).  CTA r scores the slice of `fast_per` teams starting at r * fast_per (a
+  // multiple of 4, so each slice is a whole number of 16-byte pieces) and sends its G + 1
+  // rows (the G heads' scores, then the page ids) from its list region to every CTA, row g
+  // into row g of the receive buffer [G + 1][cluster * fast_per] at the end of the ring, so
+  // that each row holds every team of the unit in team order.  In front of it,
+  // from the first stage the scratch needs: the CDF [cap] uint64, drawn flags and p [cap]
+  // 4 B each, and the sampled list (team, -log2 pi) for up to min(M, cap) teams.  The
+  // representative rows are staged from the start of the ring up to the receive buffer
+  // (peers may send while this CTA still scores; everything else is written after).
+  static constexpr int fast_per(int max_teams, int cluster) {
+    return ((max_teams + cluster - 1) / cluster + 3) / 4 * 4;
+  }
+  static constexpr size_t fast_recv_bytes(int max_teams, int cluster) {
+    return (G + 1) * static_cast<size_t>(cluster) * fast_per(max_teams, cluster) * 4;
+  }
+  static constexpr size_t fast_misc_bytes(int max_teams, int num_draws) {
+    const size_t cap = static_cast<size_t>((max_teams + 3) / 4 * 4);
+    const size_t sel = static_cast<size_t>(num_draws < max_teams ? num_draws : max_teams);
+    return (16 * cap + sizeof(ListEntry) * sel + 127) / 128 * 128;
+  }
+  static constexpr int fast_scratch_stages(int max_teams, int cluster, int num_draws) {
+    return static_cast<int>((fast_recv_bytes(max_teams, cluster) +
+                             fast_misc_bytes(max_teams, num_draws) + kStageBytes - 1) /
+                            kStageBytes);
+  }
+  // Whether a shape runs on the compact path: every team of the unit sampled in each CTA
+  // (at most 1024), slices of at most 256 teams whose scores fit the list region and whose
+  // representative rows fit in front of the receive buffer, at least one stage in front of
+  // the scratch, and each CTA's chunks within its table.
+  static constexpr bool fast_fits(int max_teams, int cluster, int team_size, int num_draws) {
+    const int per = fast_per(max_teams, cluster);
+    const int free_stages = kStages - fast_scratch_stages(max_teams, cluster, num_draws);
+    const int sel_max = num_draws < max_teams ? num_draws : max_teams;
+    const int chunks = (sel_max * (team_size / kChunk) + cluster - 1) / cluster;
+    return max_teams >= 1 && max_teams <= kMaxTeamsPerCta && per <= 256 && free_stages >= 1 &&
+           static_cast<size_t>(G + 1) * per * 4 <= sizeof(ListEntry) * kMaxTeamsPerCta &&
+           static_cast<size_t>(per) * D * 4 + fast_recv_bytes(max_teams, cluster) <=
+               static_cast<size_t>(kRing) &&
+           chunks <= kMaxChunksPerSplit;
+  }
 };
 
 // ---------------------------------------------------------------- element loaders
@@ -374,7 +417,7 @@ __device__ __forceinline__ void score_teams(const DecodeParams& p, int b, int h,
 
 // ---------------------------------------------------------------- the kernel
 
-template <bool BF16, int D, int G, bool W>
+template <bool BF16, int D, int G, bool W, bool FAST = false>
 __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks))
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using Tr = DecodeTraits<BF16, D, G, W>;
@@ -383,13 +426,13 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   cgx::cluster_group cluster = cgx::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int CL = static_cast<int>(cluster.num_blocks());
-  const int NC = p.clusters_per_unit;
+  const int NC = FAST ? 1 : p.clusters_per_unit;
   const int cidx = blockIdx.x / CL;
   const int h = blockIdx.y, b = blockIdx.z;
   const int unit = b * p.num_kv_heads + h;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, lane16 = lane & 15;
   const int M = p.num_draws;
-  const int mode = p.mode;
+  const int mode = FAST ? kModeDecode : p.mode;
   const bool sampling = mode == kModeDecode || mode == kModeSample;
   const bool attending = mode != kModeSample;
   const bool writer = cidx == 0;          // the cluster that writes the sampling outputs
@@ -408,41 +451,9 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   __shared__ int s_base[17];
   __shared__ unsigned long long s_off, s_Z;
   __shared__ int s_abort, s_last;
-  // Launched with programmatic stream serialization: nothing of global memory is touched
-  // before the previous kernel of the stream has completed, and the next one may be
-  // scheduled (onto SMs this grid leaves free) from here on.
-  if constexpr (BF16) {
-    if (attending && tid == 0) {       // descriptors are launch constants: no wait needed
-      prefetch_tensormap(&p.tmap_k);
-      prefetch_tensormap(&p.tmap_v);
-    }
-  }
-  grid_dependency_wait();
-  grid_launch_dependents();
-  if constexpr (BF16) {
-    // The 128-byte-swizzled tile copies and the fragment addressing below both assume
-    // 1 KiB-aligned stages; the layout is the same for every CTA, so all leave together.
-    if (attending && (smem_u32(smem) & 1023u) != 0) {
-      if (tid == 0 && rank == 0 && cidx == 0) set_status(p.status, SANTA_DEV_LAYOUT);
-      return;
-    }
-  }
-
-  // ---- per-unit lengths
-  const int L = p.seq_lens[b];
-  const bool len_ok = L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(p.max_teams) *
-                                                             p.team_size;
-  const int n = len_ok ? (L + p.team_size - 1) / p.team_size : 0;
-  const int cpt = p.team_size / kChunk;
-  if (!len_ok && writer && rank == 0 && tid == 0) set_status(p.status, SANTA_DEV_BAD_SEQLEN);
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
-    fence_mbar_init();
-    s_abort = 0;
-  }
-  __syncthreads();
-
+  int L = 0;                  // the unit's sequence length
+  int n_chunks = 0;           // 64-token chunks this CTA streams
+  int early_n = 0;            // chunks already issued when the chunk table is complete
   // one chunk's K and V copies into its ring stage (or a bare arrival for an empty chunk)
   const unsigned char* kpool = static_cast<const unsigned char*>(p.k_pool);
   const unsigned char* vpool = static_cast<const unsigned char*>(p.v_pool);
@@ -471,10 +482,333 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       mbar_arrive(&bar[stage]);
     }
   };
+  if constexpr (FAST) {
+    // ============================================================ compact path: phases A, B
+    // A decode step with i.i.d. draws and Horvitz-Thompson weights, no mixture, one cluster
+    // per unit, every team of the unit sampled in each CTA (DecodeTraits::fast_fits).  This
+    // code runs once per launch, so it is kept short (rolled loops) and has few phases: the
+    // SM waits on fetching straight-line instructions here more than on the arithmetic.
+    const int n_max = p.max_teams;
+    const int per = Tr::fast_per(n_max, CL);           // teams scored per CTA, multiple of 4
+    const int lo = rank * per;
+    const int nl = max(0, min(per, n_max - lo));
+    const int cap = (n_max + 3) & ~3;
+    const int sel_cap = min(M, n_max);
+    early_n = S - Tr::fast_scratch_stages(n_max, CL, M);     // stages in front of the scratch
+    const int RL = CL * per;                           // row length of the receive buffer
+    float* xs = reinterpret_cast<float*>(smem + Tr::kRing - Tr::fast_recv_bytes(n_max, CL));
+    unsigned long long* cdf = reinterpret_cast<unsigned long long*>(
+        smem + static_cast<size_t>(early_n) * Tr::kStageBytes);        // [cap]
+    int* flg = reinterpret_cast<int*>(cdf + cap);                        // [cap] drawn
+    float* ps = reinterpret_cast<float*>(flg + cap);                     // [cap] p
+    ListEntry* sel = reinterpret_cast<ListEntry*>(ps + cap);             // [sel_cap]
+    float* rows = reinterpret_cast<float*>(smem);      // [per][D] staged representatives
+    float* mine = reinterpret_cast<float*>(list);      // [G + 1][per] this CTA's slice, sent
+    int* pg = reinterpret_cast<int*>(xs + G * RL);       // [RL] page id of every team
+    uint64_t* rbar = &bar[S];                          // staged rows
+    uint64_t* xbar = &bar[S + 1];                      // the received slices
+    __shared__ int s_total;
+    const bool bad_layout = BF16 && (smem_u32(smem) & 1023u) != 0;
+    if (!bad_layout) {
+      // shared memory only: allowed before the previous kernel of the stream has finished
+      if (tid == 0) {
+        prefetch_tensormap(&p.tmap_k);
+        prefetch_tensormap(&p.tmap_v);
+        for (int s2 = 0; s2 < S; ++s2) mbar_init(&bar[s2], 1);
+        mbar_init(rbar, Tr::kThreads);
+        mbar_init(xbar, 1);
+        fence_mbar_init();
+        s_abort = 0;
+      }
+      __syncthreads();                // the mbarriers are initialised
+      if (tid == 0) mbar_arrive_expect_tx(xbar, static_cast<uint32_t>((G + 1) * RL * 4));
+      cluster_arrive_relaxed();       // split barrier: this CTA runs, its mbarriers are set up
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (bad_layout) {                 // the same for every CTA: all leave together
+      if (tid == 0 && rank == 0) set_status(p.status, SANTA_DEV_LAYOUT);
+      return;
+    }
+    // ---- the loads that depend on nothing else: length, query, this thread's row of the
+    // slice; the row's representative comes by one bulk copy on rbar
+    L = p.seq_lens[b];
+    const bool len_ok = L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(n_max) *
+                                                                p.team_size;
+    const int n = len_ok ? (L + p.team_size - 1) / p.team_size : 0;
+    if (tid < nl) {
+      const int page = p.page_table[static_cast<int64_t>(b) * n_max + lo + tid];
+      const bool ok = page >= 0 && page < p.num_pages;
+      mine[G * per + tid] = __int_as_float(ok ? page : -2);
+      if (ok) {
+        mbar_arrive_expect_tx(rbar, D * 4);
+        bulk_g2s(rows + static_cast<size_t>(tid) * D,
+                 p.reps + (static_cast<int64_t>(page) * p.num_kv_heads + h) * D, D * 4, rbar);
+      } else {
+        mbar_arrive(rbar);
+        if (lo + tid < n) set_status(p.status, SANTA_DEV_BAD_PAGE);
+      }
+    } else {
+      mbar_arrive(rbar);
+    }
+    if (!len_ok && rank == 0 && tid == 0) set_status(p.status, SANTA_DEV_BAD_SEQLEN);
+    float qs[G][Tr::kEplS];           // the group's query in the fp32 score layout
+    {
+      const uint16_t* qh = static_cast<const uint16_t*>(p.q) +
+                           (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e4 = 0; e4 < Tr::kEplS / 4; ++e4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(qh + g * D + e4 * 64 + lane16 * 4);
+          qs[g][4 * e4] = bf16_lo(w.x);
+          qs[g][4 * e4 + 1] = bf16_hi(w.x);
+          qs[g][4 * e4 + 2] = bf16_lo(w.y);
+          qs[g][4 * e4 + 3] = bf16_hi(w.y);
+        }
+    }
+    if (!mbar_wait(rbar, 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
+    // ---- the slice's scores s_{g,j} = q_g . rep_j / sqrt(d): 16 lanes per team, lane l ends
+    // with head (l >> 1) & 7; -inf past the sequence and for bad page ids
+    {
+      const int hh = (lane >> 1) & 7;
+#pragma unroll 2
+      for (int j0 = 0; j0 < nl; j0 += 16) {
+        const int jl = j0 + 2 * warp + (lane >> 4);
+        float x[Tr::kEplS];
+        if (jl < nl) {
+          load_score_row<false, D>(reinterpret_cast<const unsigned char*>(rows + static_cast<size_t>(jl) * D),
+                                   lane16, x);
+        } else {
+#pragma unroll
+          for (int e = 0; e < Tr::kEplS; ++e) x[e] = 0.f;
+        }
+        float part[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          part[g] = 0.f;
+          if (g < G) {
+#pragma unroll
+            for (int e = 0; e < Tr::kEplS; ++e) part[g] = fmaf(qs[g][e], x[e], part[g]);
+          }
+        }
+        const float sum = reduce_scatter8(part, lane);
+        if (jl < nl && !(lane & 1) && hh < G) {
+          const bool ok = __float_as_int(mine[G * per + jl]) >= 0 && lo + jl < n;
+          mine[hh * per + jl] = ok ? sum * p.scale : kNegInf;
+        }
+      }
+    }
+    // ---- send the slice to every CTA of the cluster (itself included): row g of it to
+    // row g of the receiver's buffer, one bulk copy each, completing on the receiver's xbar
+    fence_proxy_async_smem();         // slice written, staged rows read: both by the async proxy next
+    __syncthreads();
+    cluster_wait();                   // every peer runs and has initialised its mbarriers
+    if (tid < (G + 1) * CL) {
+      const int row = tid / CL, dst = tid - row * CL;
+      bulk_s2cluster(cluster_addr(smem_u32(xs + row * RL + rank * per), dst), mine + row * per,
+                     static_cast<uint32_t>(per * 4), cluster_addr(smem_u32(xbar), dst));
+    }
+    if (!mbar_wait(xbar, 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
+    // ---- per-head statistics over the unit, warp g on row g: m_g, e_gj = exp(s_gj - m_g) in
+    // place and 1 / (G z_g); four independent teams per lane at a time, summed in a fixed
+    // order (the same in every CTA)
+    const bool out_writer = rank == 0;
+    const int tpt = (n_max + Tr::kThreads - 1) / Tr::kThreads;
+    const int jt = tid * tpt;
+    __shared__ float s_zinv[kMaxGroup];
+    if (warp < G) {
+      float* row = xs + warp * RL;
+      float m = kNegInf;
+#pragma unroll 1
+      for (int j0 = lane; j0 < n_max; j0 += 128) {
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = j0 + 32 * k < n_max ? row[j0 + 32 * k] : kNegInf;
+        m = fmaxf(m, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
+      }
+      m = warp_max(m);
+      float z = 0.f;
+#pragma unroll 1
+      for (int j0 = lane; j0 < n_max; j0 += 128) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = j0 + 32 * k;
+          if (j < n_max) {
+            const float sv = row[j];
+            const float ev = sv == kNegInf ? 0.f : expf(sv - m);
+            row[j] = ev;
+            z += ev;
+          }
+        }
+      }
+      z = warp_sum(z);
+      if (lane == 0) s_zinv[warp] = z > 0.f ? 1.f / (z * static_cast<float>(G)) : 0.f;
+    }
+    __syncthreads();
+    float zg[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) zg[g] = s_zinv[g];
+    // ---- p_j = sum_g e_gj / (G z_g), round(p_j 2^62) and the exact integer CDF (this
+    // thread's inclusive sums, then one block-wide scan)
+    unsigned long long run = 0ull;
+#pragma unroll 1
+    for (int u = 0; u < tpt; ++u) {
+      const int j = jt + u;
+      if (j < n_max) {
+        float pj = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) pj = fmaf(xs[g * RL + j], zg[g], pj);
+        unsigned long long P = 0ull;
+        if (pj > 0.f) {
+          const float x = pj * 0x1p62f;                              // exact scaling
+          const unsigned long long fl = __float2ull_rd(x);
+          const float frac = x - __ull2float_rn(fl);                 // exact
+          P = fl + (frac >= 0.5f ? 1ull : 0ull);
+        }
+        run += P;
+        cdf[j] = run;                 // this thread's inclusive sum; its prefix is added below
+        ps[j] = pj;
+        flg[j] = 0;
+        if (p.team_probs && out_writer)
+          p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = pj;
+      }
+    }
+    unsigned long long Z;
+    const unsigned long long before = block_exclusive_scan<unsigned long long>(run, s_wd, Z);
+#pragma unroll 1
+    for (int u = 0; u < tpt; ++u)
+      if (jt + u < n_max) cdf[jt + u] += before;
+    __syncthreads();
+    // ---- M draws: the smallest j with floor(u Z) < C_j
+    const bool valid = len_ok && Z > 0ull;
+    if (valid) {
+      const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
+                                   static_cast<uint32_t>(p.seed >> 32));
+#pragma unroll 1
+      for (int r = tid; r < M; r += Tr::kThreads) {
+        const uint4 w = philox4x32_10_compact(make_uint4(static_cast<uint32_t>(r),
+                                                         static_cast<uint32_t>(h),
+                                                         static_cast<uint32_t>(b), 0u), key);
+        const unsigned long long a = 2ull * w.x + 1ull;              // u = a / 2^33
+        const unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
+        int lo_i = 0, hi_i = n_max - 1;
+#pragma unroll 1
+        while (lo_i < hi_i) {
+          const int mid = (lo_i + hi_i) >> 1;
+          if (t < cdf[mid]) hi_i = mid; else lo_i = mid + 1;
+        }
+        if (out_writer) p.draw_ids[static_cast<int64_t>(unit) * M + r] = lo_i;
+        flg[lo_i] = 1;
+      }
+    } else if (out_writer) {
+#pragma unroll 1
+      for (int r = tid; r < M; r += Tr::kThreads) p.draw_ids[static_cast<int64_t>(unit) * M + r] = -1;
+    }
+    // pi_j = 1 - (1 - p_j)^M and the weight -log2 pi_j of every team, threads in reverse order
+    // (those that drew nothing take the first teams): ps becomes pi, and the weight goes to
+    // the first score row of the received slices, no longer read
+    {
+      const float Mf = static_cast<float>(M);
+#pragma unroll 1
+      for (int j = Tr::kThreads - 1 - tid; j < n_max; j += Tr::kThreads) {
+        const float piv = -expm1f(Mf * log1pf(-ps[j]));
+        ps[j] = piv;
+        xs[j] = -log2f(piv);
+      }
+    }
+    __syncthreads();
+    // ---- S in ascending team order: per-thread counts, a block scan, one slot per team
+    {
+      int cnt = 0;
+#pragma unroll 1
+      for (int u = 0; u < tpt; ++u) cnt += (jt + u < n_max && flg[jt + u]) ? 1 : 0;
+      int tot;
+      int k = block_exclusive_scan<int>(cnt, s_wi, tot);
+#pragma unroll 1
+      for (int u = 0; u < tpt; ++u) {
+        const int j = jt + u;
+        if (j < n_max && flg[j]) {
+          sel[k] = ListEntry{j, xs[j]};
+          if (out_writer) {
+            p.sel_ids[static_cast<int64_t>(unit) * M + k] = j;
+            p.pi[static_cast<int64_t>(unit) * M + k] = ps[j];
+          }
+          ++k;
+        }
+      }
+      if (out_writer) {
+#pragma unroll 1
+        for (int k2 = tot + tid; k2 < M; k2 += Tr::kThreads) {
+          p.sel_ids[static_cast<int64_t>(unit) * M + k2] = -1;
+          p.pi[static_cast<int64_t>(unit) * M + k2] = 0.f;
+        }
+        if (tid == 0) p.sel_count[unit] = tot;
+      }
+      if (tid == 0) s_total = min(tot, sel_cap);
+    }
+    __syncthreads();
+    // ---- phase B: this CTA's contiguous range of the sampled teams' 64-token chunks; the
+    // first early_n go to the stages in front of the scratch at once
+    {
+      const int cpt = p.team_size / kChunk;
+      const int total_chunks = s_total * cpt;
+      const int cps = (total_chunks + CL - 1) / CL;
+      const int c_begin = min(rank * cps, total_chunks);
+      n_chunks = min(total_chunks - c_begin, cps);
+#pragma unroll 1
+      for (int ci = tid; ci < n_chunks; ci += Tr::kThreads) {
+        const int c = c_begin + ci, slot = c / cpt, part = c - slot * cpt;
+        const ListEntry e = sel[slot];
+        const int page = pg[e.team];
+        const bool pok = page >= 0 && page < p.num_pages;
+        const int vt = pok ? max(0, min(min(p.team_size, L - e.team * p.team_size) -
+                                            part * kChunk, kChunk))
+                           : 0;
+        const ChunkMeta m{vt > 0 ? page : -1, vt, e.lw2, part};
+        table[ci] = m;
+        if (ci < early_n) issue_meta(ci, m);
+      }
+    }
+  } else {
+  // Launched with programmatic stream serialization: nothing of global memory is touched
+  // before the previous kernel of the stream has completed, and the next one may be
+  // scheduled (onto SMs this grid leaves free) from here on.
+  if constexpr (BF16) {
+    if (attending && tid == 0) {       // descriptors are launch constants: no wait needed
+      prefetch_tensormap(&p.tmap_k);
+      prefetch_tensormap(&p.tmap_v);
+    }
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if constexpr (BF16) {
+    // The 128-byte-swizzled tile copies and the fragment addressing below both assume
+    // 1 KiB-aligned stages; the layout is the same for every CTA, so all leave together.
+    if (attending && (smem_u32(smem) & 1023u) != 0) {
+      if (tid == 0 && rank == 0 && cidx == 0) set_status(p.status, SANTA_DEV_LAYOUT);
+      return;
+    }
+  }
+
+  // ---- per-unit lengths
+  L = p.seq_lens[b];
+  const bool len_ok = L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(p.max_teams) *
+                                                             p.team_size;
+  const int n = len_ok ? (L + p.team_size - 1) / p.team_size : 0;
+  const int cpt = p.team_size / kChunk;
+  if (!len_ok && writer && rank == 0 && tid == 0) set_status(p.status, SANTA_DEV_BAD_SEQLEN);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+
   // Decode steps sampled inside one CTA keep the phase-A scratch in the last stage(s) of the
   // ring, so that this CTA's first `early_n` chunks can be copied as soon as S is known,
   // while the chunk table is still being built from that scratch.
-  int early_n = 0;
 
   // ================================================================ phase A: sampling
   int total_sel = 0;                      // |S| of the unit
@@ -894,7 +1228,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   const int total_chunks = attending ? total_sel * cpt : 0;
   const int cps = (total_chunks + ctas - 1) / ctas;
   const int c_begin = min(gidx * cps, total_chunks);
-  const int n_chunks = min(total_chunks - c_begin, cps);
+  n_chunks = min(total_chunks - c_begin, cps);
   const float Mf = static_cast<float>(M);
   if (lmask && writer && rank == 0) {
     // the sampling outputs of the unit: S in ascending order with pi, padded
@@ -947,6 +1281,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     const int vt =
         ok ? max(0, min(min(p.team_size, L - team * p.team_size) - part * kChunk, kChunk)) : 0;
     table[ci] = ChunkMeta{vt > 0 ? page : -1, vt, lw2, part};
+  }
   }
   fence_proxy_async_smem();      // the ring held phase-A scratch; the copies overwrite it
   __syncthreads();
@@ -1541,7 +1876,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   __threadfence();
   __syncthreads();
   if (tid == 0)
-    s_last = atomicAdd(&p.counters[unit], 1u) == static_cast<unsigned>(ctas - 1);
+    s_last = atomicAdd(&p.counters[unit], 1u) == static_cast<unsigned>(CL * NC - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -1584,18 +1919,18 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
 
 // ---------------------------------------------------------------- host-side launch helpers
 
-template <bool BF16, int D, int G, bool W>
+template <bool BF16, int D, int G, bool W, bool FAST = false>
 std::atomic<unsigned long long>& decode_smem_flag() {
   static std::atomic<unsigned long long> flag{0};
   return flag;
 }
 
-template <bool BF16, int D, int G, bool W>
+template <bool BF16, int D, int G, bool W, bool FAST = false>
 cudaError_t decode_prepare_t() {
   using Tr = DecodeTraits<BF16, D, G, W>;
-  auto* kern = decode_kernel<BF16, D, G, W>;
+  auto* kern = decode_kernel<BF16, D, G, W, FAST>;
   static std::atomic<unsigned long long> cluster_flag{0};
-  cudaError_t e = ensure_dynamic_smem(kern, Tr::kSmem, decode_smem_flag<BF16, D, G, W>());
+  cudaError_t e = ensure_dynamic_smem(kern, Tr::kSmem, decode_smem_flag<BF16, D, G, W, FAST>());
   if (e != cudaSuccess) return e;
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1609,10 +1944,10 @@ cudaError_t decode_prepare_t() {
 }
 
 // How many clusters of `cluster` CTAs can be co-resident (0 if none / on error).
-template <bool BF16, int D, int G, bool W>
+template <bool BF16, int D, int G, bool W, bool FAST = false>
 int decode_max_clusters_t(int cluster) {
   using Tr = DecodeTraits<BF16, D, G, W>;
-  if (decode_prepare_t<BF16, D, G, W>() != cudaSuccess) return 0;
+  if (decode_prepare_t<BF16, D, G, W, FAST>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, 1, 1);
   cfg.blockDim = dim3(Tr::kThreads);
@@ -1625,26 +1960,26 @@ int decode_max_clusters_t(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<BF16, D, G, W>, &cfg) != cudaSuccess)
+  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<BF16, D, G, W, FAST>, &cfg) != cudaSuccess)
     return 0;
   return n;
 }
 
-template <bool BF16, int D, int G, bool W>
+template <bool BF16, int D, int G, bool W, bool FAST = false>
 int decode_resident_t() {
   using Tr = DecodeTraits<BF16, D, G, W>;
-  if (decode_prepare_t<BF16, D, G, W>() != cudaSuccess) return 0;
+  if (decode_prepare_t<BF16, D, G, W, FAST>() != cudaSuccess) return 0;
   int blocks = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, decode_kernel<BF16, D, G, W>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, decode_kernel<BF16, D, G, W, FAST>,
                                                     Tr::kThreads, Tr::kSmem) != cudaSuccess)
     return 0;
   return blocks;
 }
 
-template <bool BF16, int D, int G, bool W>
+template <bool BF16, int D, int G, bool W, bool FAST = false>
 cudaError_t decode_launch_t(const DecodeParams& p, dim3 grid, int cluster, cudaStream_t stream) {
   using Tr = DecodeTraits<BF16, D, G, W>;
-  cudaError_t e = decode_prepare_t<BF16, D, G, W>();
+  cudaError_t e = decode_prepare_t<BF16, D, G, W, FAST>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -1662,7 +1997,7 @@ cudaError_t decode_launch_t(const DecodeParams& p, dim3 grid, int cluster, cudaS
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<BF16, D, G, W>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<BF16, D, G, W, FAST>, p);
 }
 
 // Dispatch on the group size (1..8) for one (dtype, head_dim).

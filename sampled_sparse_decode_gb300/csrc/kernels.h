@@ -127,6 +127,17 @@ cudaError_t decode_launch_bf16_wide(const DecodeParams& p, int head_dim, int gro
                                     int cluster, cudaStream_t stream);
 int decode_resident_bf16_wide(int head_dim, int group);
 int decode_max_clusters_bf16_wide(int head_dim, int group, int cluster);
+// compact path (bf16 decode steps with i.i.d. Horvitz-Thompson draws, no mixture, one
+// cluster per unit, every team sampled in each CTA): launchers of both variants and the
+// shape test; same shared memory and resident CTAs as the general kernel of each variant
+cudaError_t decode_launch_bf16_fast(const DecodeParams& p, int head_dim, int group, dim3 grid,
+                                    int cluster, cudaStream_t stream);
+cudaError_t decode_launch_bf16_wide_fast(const DecodeParams& p, int head_dim, int group,
+                                         dim3 grid, int cluster, cudaStream_t stream);
+bool decode_fast_fits_bf16(int head_dim, int group, int max_teams, int cluster, int team_size,
+                           int num_draws);
+bool decode_fast_fits_bf16_wide(int head_dim, int group, int max_teams, int cluster,
+                                int team_size, int num_draws);
 
 // Every host-side check santa_decode makes on `a`, then its launch plan; launches nothing
 // and touches no device memory.  On SANTA_OK *clusters_per_unit receives the plan's NC (> 1:

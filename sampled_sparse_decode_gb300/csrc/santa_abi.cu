@@ -216,8 +216,12 @@ int choose_variant(int dtype, int64_t units, int G, int d, int T, int max_teams,
   const int64_t sms = current_sms();
   if (units * pl->cluster * pl->clusters > sms) return SANTA_OK;
   Plan w;
+  // a sampling step scores ceil(max_teams / CL) teams per CTA before any K/V arrives: it
+  // keeps the larger cluster when the wide variant's would leave a CTA more than 64 teams
   if (choose(dtype, units, G, d, T, max_teams, M, mode, nc_cap, true, &w) == SANTA_OK &&
-      units * w.cluster * w.clusters <= sms)
+      units * w.cluster * w.clusters <= sms &&
+      (mode != santa::kModeDecode || w.cluster >= pl->cluster ||
+       ceil_div(max_teams, w.cluster) <= 64))
     *pl = w;
   return SANTA_OK;
 }
@@ -294,6 +298,19 @@ int encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int d) {
   return r == CUDA_SUCCESS ? SANTA_OK : SANTA_ERR_CUDA;
 }
 
+// Whether a checked and planned call runs the compact path of the decode kernel: a bf16
+// decode step with i.i.d. Horvitz-Thompson draws, no mixture and one cluster per unit, whose
+// shape the compact path's shared-memory layout holds.
+bool uses_compact_path(const santa_decode_args* a, int mode, const Plan& pl) {
+  if (mode != santa::kModeDecode || a->dtype != SANTA_BF16 || pl.clusters != 1) return false;
+  if (a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f) return false;
+  const int G = a->num_q_heads / a->num_kv_heads;
+  return pl.wide ? santa::decode_fast_fits_bf16_wide(a->head_dim, G, a->max_teams, pl.cluster,
+                                                     a->team_size, a->num_draws)
+                 : santa::decode_fast_fits_bf16(a->head_dim, G, a->max_teams, pl.cluster,
+                                                a->team_size, a->num_draws);
+}
+
 // Every host-side check of a call in `mode`, then its plan; launches nothing.
 int check_and_plan(const santa_decode_args* a, int mode, Plan* pl) {
   int rc = check_inputs(a);
@@ -365,6 +382,12 @@ int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   }
   const dim3 grid(pl.cluster * pl.clusters, a->num_kv_heads, a->batch);
   const int G = a->num_q_heads / a->num_kv_heads;
+  if (uses_compact_path(a, mode, pl)) {
+    return map_cuda(pl.wide ? santa::decode_launch_bf16_wide_fast(p, a->head_dim, G, grid,
+                                                                  pl.cluster, stream)
+                            : santa::decode_launch_bf16_fast(p, a->head_dim, G, grid,
+                                                             pl.cluster, stream));
+  }
   const cudaError_t e =
       a->dtype == SANTA_BF16
           ? (pl.wide ? santa::decode_launch_bf16_wide(p, a->head_dim, G, grid, pl.cluster, stream)
@@ -585,6 +608,17 @@ int santa_decode_plan(const santa_decode_args* a, int which, int32_t* out) {
                         pl.cluster, pl.wide);
   out[4] = pl.wide ? 1 : 0;
   return SANTA_OK;
+}
+
+int santa_decode_path(const santa_decode_args* a) {
+  if (!a) return -SANTA_ERR_INVALID_ARG;
+  int rc = check_shape(a->dtype, a->batch, a->num_q_heads, a->num_kv_heads, a->head_dim,
+                       a->team_size, a->max_teams);
+  if (rc) return -rc;
+  if (a->num_draws < 1 || a->num_draws > kMaxDraws) return -SANTA_ERR_UNSUPPORTED;
+  Plan pl;
+  if ((rc = make_plan(a, santa::kModeDecode, &pl))) return -rc;
+  return uses_compact_path(a, santa::kModeDecode, pl) ? 1 : 0;
 }
 
 int santa_sample(const santa_decode_args* a, void* stream) {

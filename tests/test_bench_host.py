@@ -66,3 +66,33 @@ def test_mean_ci(bench):
     sd = math.sqrt(sum((x - 2.5) ** 2 for x in xs) / 3)
     assert m == 2.5 and abs(ci - 1.96 * sd / 2.0) < 1e-12
     assert bench._mean_ci([5.0]) == (5.0, 0.0)
+
+
+def test_traffic_record_from_an_ncu_log(bench, tmp_path):
+    """--record-traffic reads ncu's one-row-per-metric CSV (units scaled or in bytes), keeps
+    the decode launches only, and keys the record by the current kernel sources' hash."""
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+           '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+           '"Metric Value"\n')
+
+    def row(i, kern, metric, unit, val):
+        return (f'"{i}","1","python","h","{kern}","1","7","(256, 1, 1)","(16, 4, 1)","0",'
+                f'"10.3","Command line profiler metrics","{metric}","{unit}","{val}"\n')
+
+    k = "void santa::decode_kernel<true, 128, 7, true>(santa::DecodeParams)"
+    text = ("==PROF== Connected to process 1\n" + hdr +
+            row(0, k, "dram__bytes_read.sum", "Mbyte", "8.17") +
+            row(0, k, "dram__bytes_write.sum", "byte", "0") +
+            row(1, "void at::native::fill_kernel()", "dram__bytes_read.sum", "byte", "5") +
+            row(1, "void at::native::fill_kernel()", "dram__bytes_write.sum", "byte", "5") +
+            row(2, k, "dram__bytes_read.sum", "byte", "7,915,008") +
+            row(2, k, "dram__bytes_write.sum", "Kbyte", "1.5"))
+    csv_path = tmp_path / "traffic.csv"
+    csv_path.write_text(text)
+    out = tmp_path / "rec.json"
+    rec = bench.record_traffic_file(str(csv_path), str(out), "w", "ncu ...")
+    assert rec["dram_bytes_read_per_launch"] == [8.17e6, 7915008.0]
+    assert rec["dram_bytes_write_per_launch"] == [0.0, 1500.0]
+    assert rec["dram_bytes_per_launch"] == (8.17e6 + 7915008.0 + 1500.0) / 2
+    assert rec["kernel_source_sha"] == bench.kernel_source_sha()
+    assert json.loads(out.read_text()) == rec

@@ -68,6 +68,30 @@ def test_both_kernel_variants_are_covered():
                                            "sample")["wide"]
 
 
+def test_compact_and_general_forms_are_both_covered():
+    """bf16 decode steps with the default sampler run the compact form of the kernel (both
+    variants); fp32 steps, sampler variants, a mixture and units spread over several clusters
+    run the general form.  The parity tests below cover each."""
+    cases = [("qwen_b2_ragged", {}, "compact"), ("bf16_d64_t64", {}, "compact"),
+             ("qwen_b40_two_per_sm", {}, "compact"), ("llama_paged_b4", {}, "compact"),
+             ("long_paged_b2", {}, "compact"), ("qwen_b3_mixed_m64", {}, "compact"),
+             ("long_b1_multicluster", {}, "compact"),
+             ("tiny_f32", {}, "general"), ("f32_d128_g8", {}, "general"),
+             ("f32_b1_two_clusters", {}, "general"),
+             ("qwen_b2_ragged", dict(sampler="systematic"), "general"),
+             ("qwen_b2_ragged", dict(mix_alpha=0.05), "general")]
+    for name, kw, want in cases:
+        wl = make(SMALL[name])
+        dw = DeviceWorkload(wl)
+        got = santa.santa_decode_path(dw.q, dw.k_pool, dw.page_table, wl.cfg.draws, **kw)
+        assert got == want, (name, kw, got)
+    for name in FULL:
+        wl = full_workload(name)
+        dw = DeviceWorkload(wl)
+        assert santa.santa_decode_path(dw.q, dw.k_pool, dw.page_table, wl.cfg.draws) == \
+            "compact", name
+
+
 def make(spec, **extra):
     spec = dict(spec, **extra)
     name = spec.pop("cfg")
@@ -224,10 +248,20 @@ def test_seed_sweep_draws_bit_exact():
 FULL = ["qwen7b_32k_b1_m31", "qwen7b_32k_b8_m64", "llama8b_paged_32k_b16_m32", "long_128k_b4_m64"]
 
 
+def spread_units(batch, kv_heads, n=8):
+    """Up to n (sequence, KV head) units spread evenly over the batch and the heads."""
+    idx = np.unique(np.linspace(0, batch * kv_heads - 1, min(n, batch * kv_heads)).round())
+    return [(int(i) // kv_heads, int(i) % kv_heads) for i in idx]
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled_units(name):
-    """Full-size workloads in the launch configuration the benchmark times (santa_decode with
-    the default workspace); the oracle checks a sample of units one by one."""
+    """Full-size workloads in the launch configuration the benchmark times (santa_decode and
+    santa_attend with the default workspace).  On up to 8 units spread over the batch and
+    the heads, the oracle checks p, the draws, S and pi; santa_attend is then fed the
+    oracle's own S and pi for those units (the GPU's for the others, so the launch is the
+    full one) and its outputs are compared with the oracle's on the same sets; the fused
+    step's outputs are compared wherever its sets equal the oracle's (at least one unit)."""
     wl = full_workload(name)
     cfg = wl.cfg
     dw = DeviceWorkload(wl)
@@ -239,16 +273,34 @@ def test_full_size_sampled_units(name):
                               cfg.draws, seed, team_probs=True)
     torch.cuda.synchronize()
     assert bufs.status() == 0
-    units = sorted({(0, 0), (cfg.batch // 2, cfg.kv_heads // 2),
-                    (cfg.batch - 1, cfg.kv_heads - 1)})
+    units = spread_units(cfg.batch, cfg.kv_heads)
+    assert len(units) == min(8, cfg.batch * cfg.kv_heads)
     tol = TOL_OUT[cfg.dtype]
+    sel_t, cnt_t, pi_t = bufs.sel_ids.clone(), bufs.sel_count.clone(), bufs.pi.clone()
+    oracle_sets = {}
+    fused_checked = 0
     for b, h in units:
         check_unit_sampling(wl, pr, reps_o, bufs, cfg.draws, seed, b, h)
         p = oracle.team_probs(pr, reps_o, b, h)
         d, _, _ = oracle.draw(p, cfg.draws, seed, b, h)
         s, pi = oracle.select(d, p)
-        if np.array_equal(bufs.sel_ids[b, h, :s.size].cpu().numpy(), s):
+        oracle_sets[(b, h)] = (s, pi)
+        sel_t[b, h] = -1
+        sel_t[b, h, :s.size] = torch.from_numpy(s).cuda()
+        cnt_t[b, h] = s.size
+        pi_t[b, h] = 0.0
+        pi_t[b, h, :s.size] = torch.from_numpy(pi.astype(np.float32)).cuda()
+        if int(bufs.sel_count[b, h]) == s.size and np.array_equal(
+                bufs.sel_ids[b, h, :s.size].cpu().numpy(), s):
             check_unit_attend(wl, pr, dw, b, h, s, pi, bufs.out, tol)
+            fused_checked += 1
+    assert fused_checked >= 1
+    ab = santa.santa_attend(dw.q, dw.k_pool, dw.v_pool, dw.page_table, dw.seq_lens, sel_t,
+                            cnt_t, pi_t)
+    torch.cuda.synchronize()
+    assert ab.status() == 0
+    for (b, h), (s, pi) in oracle_sets.items():
+        check_unit_attend(wl, pr, dw, b, h, s, pi, ab.out, tol)
     # properties that hold for every unit at any size
     cnt = bufs.sel_count.cpu().numpy()
     assert (cnt >= 1).all() and (cnt <= min(cfg.draws, cfg.n_teams)).all()

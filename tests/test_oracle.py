@@ -242,6 +242,42 @@ def test_draws_are_exact_on_the_integer_cdf():
             assert draws[r] == bisect.bisect_right(C, tr)
 
 
+def test_draws_follow_the_plain_definition_on_the_unrounded_probabilities():
+    """The fixed-point draws against the method's plain definition, taken exactly: with the
+    fp64 probabilities p as exact rationals, C_i = p_0 + ... + p_i, Z = C_{n-1} and
+    u = (x + 1/2) / 2^32 (x the draw's Philox word), draw r is the smallest i with
+    u Z < C_i ("sample M teams with probability p_i", explainer section 三 step 3).  The
+    62-bit rounding of p may move a draw only across a boundary that u Z lies within
+    1e-12 Z of; such draws are counted and must be rare, every other draw must agree."""
+    import bisect
+    from fractions import Fraction
+    rng = np.random.default_rng(17)
+    near, total = 0, 0
+    for n, M, seed, b, h in [(5, 400, 9, 0, 0), (64, 800, 2**33 + 1, 2, 1),
+                             (256, 1000, 31, 0, 3), (1024, 600, 123456789, 5, 0)]:
+        p = rng.dirichlet(np.full(n, 0.5))
+        p[rng.integers(0, n, size=max(1, n // 16))] = 0.0          # empty teams
+        p[rng.integers(0, n)] = 1e-300                              # far below 2^-62
+        C, acc = [], Fraction(0)
+        for x in p:
+            acc += Fraction(float(x))
+            C.append(acc)
+        Z = C[-1]
+        draws, _, _ = oracle.draw(p, M, seed, b, h)
+        for r in range(M):
+            x = int(oracle.philox4x32_10([r, h, b, 0], [seed & 0xFFFFFFFF, seed >> 32])[0])
+            uZ = Fraction(2 * x + 1, 2**33) * Z
+            plain = bisect.bisect_right(C, uZ)        # smallest i with uZ < C_i
+            total += 1
+            if draws[r] != plain:
+                lo, hi = sorted((int(draws[r]), plain))
+                gap = min(abs(uZ - C[i]) for i in range(lo, hi))
+                assert gap <= Fraction(1, 10**12) * Z, (n, r, draws[r], plain, float(gap / Z))
+                near += 1
+            assert p[draws[r]] > 0.0                  # an empty team is never drawn
+    assert near <= 1e-4 * total, (near, total)
+
+
 def test_draw_frequencies_follow_p():
     """Chi-square goodness of fit of 200000 draws to p; a zero-probability team is never
     drawn (an off-by-one in the inverse CDF shifts mass and fails this)."""
