@@ -25,4 +25,9 @@ bool decode_fast_fits_bf16_wide(int head_dim, int group, int max_teams, int clus
                                       max_teams, cluster, team_size, num_draws)))
 }
 
+int decode_resident_bf16_wide_fast(int head_dim, int group) {
+  if (head_dim == 128) { SANTA_DISPATCH_G(group, return (decode_resident_t<true, 128, GG, true, true>())) }
+  SANTA_DISPATCH_G(group, return (decode_resident_t<true, 64, GG, true, true>()))
+}
+
 }  // namespace santa

@@ -133,26 +133,23 @@ struct DecodeTraits {
   // multiple of 4, so each slice is a whole number of 16-byte pieces) and sends its G + 1
   // rows (the G heads' scores, then the page ids) from its list region to every CTA, row g
   // into row g of the receive buffer [G + 1][cluster * fast_per] at the end of the ring, so
-  // that each row holds every team of the unit in team order.  In front of it,
-  // from the first stage the scratch needs: the CDF [cap] uint64, drawn flags and p [cap]
-  // 4 B each, and the sampled list (team, -log2 pi) for up to min(M, cap) teams.  The
-  // representative rows are staged from the start of the ring up to the receive buffer
-  // (peers may send while this CTA still scores; everything else is written after).
+  // that each row holds every team of the unit in team order.  In front of it, from the
+  // first stage the scratch needs: the CDF [cap] uint64, drawn flags and p (then pi) [cap]
+  // 4 B each.  The representative rows are staged from the start of the ring up to the
+  // receive buffer (peers may send while this CTA still scores; everything else is written
+  // after).
   static constexpr int fast_per(int max_teams, int cluster) {
     return ((max_teams + cluster - 1) / cluster + 3) / 4 * 4;
   }
   static constexpr size_t fast_recv_bytes(int max_teams, int cluster) {
     return (G + 1) * static_cast<size_t>(cluster) * fast_per(max_teams, cluster) * 4;
   }
-  static constexpr size_t fast_misc_bytes(int max_teams, int num_draws) {
-    const size_t cap = static_cast<size_t>((max_teams + 3) / 4 * 4);
-    const size_t sel = static_cast<size_t>(num_draws < max_teams ? num_draws : max_teams);
-    return (16 * cap + sizeof(ListEntry) * sel + 127) / 128 * 128;
+  static constexpr size_t fast_misc_bytes(int max_teams) {
+    return (16 * static_cast<size_t>((max_teams + 3) / 4 * 4) + 127) / 128 * 128;
   }
-  static constexpr int fast_scratch_stages(int max_teams, int cluster, int num_draws) {
-    return static_cast<int>((fast_recv_bytes(max_teams, cluster) +
-                             fast_misc_bytes(max_teams, num_draws) + kStageBytes - 1) /
-                            kStageBytes);
+  static constexpr int fast_scratch_stages(int max_teams, int cluster) {
+    return static_cast<int>((fast_recv_bytes(max_teams, cluster) + fast_misc_bytes(max_teams) +
+                             kStageBytes - 1) / kStageBytes);
   }
   // Whether a shape runs on the compact path: every team of the unit sampled in each CTA
   // (at most 1024), slices of at most 256 teams whose scores fit the list region and whose
@@ -160,7 +157,7 @@ struct DecodeTraits {
   // the scratch, and each CTA's chunks within its table.
   static constexpr bool fast_fits(int max_teams, int cluster, int team_size, int num_draws) {
     const int per = fast_per(max_teams, cluster);
-    const int free_stages = kStages - fast_scratch_stages(max_teams, cluster, num_draws);
+    const int free_stages = kStages - fast_scratch_stages(max_teams, cluster);
     const int sel_max = num_draws < max_teams ? num_draws : max_teams;
     const int chunks = (sel_max * (team_size / kChunk) + cluster - 1) / cluster;
     return max_teams >= 1 && max_teams <= kMaxTeamsPerCta && per <= 256 && free_stages >= 1 &&
@@ -493,21 +490,18 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     const int lo = rank * per;
     const int nl = max(0, min(per, n_max - lo));
     const int cap = (n_max + 3) & ~3;
-    const int sel_cap = min(M, n_max);
-    early_n = S - Tr::fast_scratch_stages(n_max, CL, M);     // stages in front of the scratch
+    early_n = S - Tr::fast_scratch_stages(n_max, CL);     // stages in front of the scratch
     const int RL = CL * per;                           // row length of the receive buffer
     float* xs = reinterpret_cast<float*>(smem + Tr::kRing - Tr::fast_recv_bytes(n_max, CL));
     unsigned long long* cdf = reinterpret_cast<unsigned long long*>(
         smem + static_cast<size_t>(early_n) * Tr::kStageBytes);        // [cap]
     int* flg = reinterpret_cast<int*>(cdf + cap);                        // [cap] drawn
     float* ps = reinterpret_cast<float*>(flg + cap);                     // [cap] p
-    ListEntry* sel = reinterpret_cast<ListEntry*>(ps + cap);             // [sel_cap]
     float* rows = reinterpret_cast<float*>(smem);      // [per][D] staged representatives
     float* mine = reinterpret_cast<float*>(list);      // [G + 1][per] this CTA's slice, sent
     int* pg = reinterpret_cast<int*>(xs + G * RL);       // [RL] page id of every team
     uint64_t* rbar = &bar[S];                          // staged rows
     uint64_t* xbar = &bar[S + 1];                      // the received slices
-    __shared__ int s_total;
     const bool bad_layout = BF16 && (smem_u32(smem) & 1023u) != 0;
     if (!bad_layout) {
       // shared memory only: allowed before the previous kernel of the stream has finished
@@ -609,6 +603,15 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       bulk_s2cluster(cluster_addr(smem_u32(xs + row * RL + rank * per), dst), mine + row * per,
                      static_cast<uint32_t>(per * 4), cluster_addr(smem_u32(xbar), dst));
     }
+    // the Philox word of draw tid (it needs nothing else) while the slices arrive; kept in
+    // shared memory so that it is computed here and not next to its use
+    __shared__ uint32_t s_xw[Tr::kThreads];
+    const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
+                                 static_cast<uint32_t>(p.seed >> 32));
+    if (tid < M)
+      s_xw[tid] = philox4x32_10_compact(make_uint4(static_cast<uint32_t>(tid),
+                                                   static_cast<uint32_t>(h),
+                                                   static_cast<uint32_t>(b), 0u), key).x;
     if (!mbar_wait(xbar, 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
     // ---- per-head statistics over the unit, warp g on row g: m_g, e_gj = exp(s_gj - m_g) in
     // place and 1 / (G z_g); four independent teams per lane at a time, summed in a fixed
@@ -683,14 +686,14 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     // ---- M draws: the smallest j with floor(u Z) < C_j
     const bool valid = len_ok && Z > 0ull;
     if (valid) {
-      const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
-                                   static_cast<uint32_t>(p.seed >> 32));
 #pragma unroll 1
       for (int r = tid; r < M; r += Tr::kThreads) {
-        const uint4 w = philox4x32_10_compact(make_uint4(static_cast<uint32_t>(r),
-                                                         static_cast<uint32_t>(h),
-                                                         static_cast<uint32_t>(b), 0u), key);
-        const unsigned long long a = 2ull * w.x + 1ull;              // u = a / 2^33
+        const uint32_t x = r == tid ? s_xw[r]
+                                    : philox4x32_10_compact(make_uint4(static_cast<uint32_t>(r),
+                                                                       static_cast<uint32_t>(h),
+                                                                       static_cast<uint32_t>(b), 0u),
+                                                            key).x;
+        const unsigned long long a = 2ull * x + 1ull;                // u = a / 2^33
         const unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
         int lo_i = 0, hi_i = n_max - 1;
 #pragma unroll 1
@@ -718,21 +721,42 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       }
     }
     __syncthreads();
-    // ---- S in ascending team order: per-thread counts, a block scan, one slot per team
+    // ---- S in ascending team order (per-thread counts, a block scan: slot k of each drawn
+    // team) and phase B at once: the thread holding a sampled team writes its outputs and the
+    // table entries of its 64-token chunks that fall in this CTA's contiguous range, and
+    // copies at once those that go to the stages in front of the scratch
     {
       int cnt = 0;
 #pragma unroll 1
       for (int u = 0; u < tpt; ++u) cnt += (jt + u < n_max && flg[jt + u]) ? 1 : 0;
       int tot;
       int k = block_exclusive_scan<int>(cnt, s_wi, tot);
+      const int cpt = p.team_size / kChunk;
+      const int total_chunks = tot * cpt;
+      const int cps = (total_chunks + CL - 1) / CL;
+      const int c_begin = min(rank * cps, total_chunks);
+      n_chunks = min(total_chunks - c_begin, cps);
 #pragma unroll 1
       for (int u = 0; u < tpt; ++u) {
         const int j = jt + u;
         if (j < n_max && flg[j]) {
-          sel[k] = ListEntry{j, xs[j]};
           if (out_writer) {
             p.sel_ids[static_cast<int64_t>(unit) * M + k] = j;
             p.pi[static_cast<int64_t>(unit) * M + k] = ps[j];
+          }
+          const int page = pg[j];
+          const bool pok = page >= 0 && page < p.num_pages;
+#pragma unroll 1
+          for (int part = 0; part < cpt; ++part) {
+            const int ci = k * cpt + part - c_begin;
+            if (ci >= 0 && ci < n_chunks) {
+              const int vt = pok ? max(0, min(min(p.team_size, L - j * p.team_size) -
+                                                  part * kChunk, kChunk))
+                                 : 0;
+              const ChunkMeta m{vt > 0 ? page : -1, vt, xs[j], part};
+              table[ci] = m;
+              if (ci < early_n) issue_meta(ci, m);
+            }
           }
           ++k;
         }
@@ -744,30 +768,6 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
           p.pi[static_cast<int64_t>(unit) * M + k2] = 0.f;
         }
         if (tid == 0) p.sel_count[unit] = tot;
-      }
-      if (tid == 0) s_total = min(tot, sel_cap);
-    }
-    __syncthreads();
-    // ---- phase B: this CTA's contiguous range of the sampled teams' 64-token chunks; the
-    // first early_n go to the stages in front of the scratch at once
-    {
-      const int cpt = p.team_size / kChunk;
-      const int total_chunks = s_total * cpt;
-      const int cps = (total_chunks + CL - 1) / CL;
-      const int c_begin = min(rank * cps, total_chunks);
-      n_chunks = min(total_chunks - c_begin, cps);
-#pragma unroll 1
-      for (int ci = tid; ci < n_chunks; ci += Tr::kThreads) {
-        const int c = c_begin + ci, slot = c / cpt, part = c - slot * cpt;
-        const ListEntry e = sel[slot];
-        const int page = pg[e.team];
-        const bool pok = page >= 0 && page < p.num_pages;
-        const int vt = pok ? max(0, min(min(p.team_size, L - e.team * p.team_size) -
-                                            part * kChunk, kChunk))
-                           : 0;
-        const ChunkMeta m{vt > 0 ? page : -1, vt, e.lw2, part};
-        table[ci] = m;
-        if (ci < early_n) issue_meta(ci, m);
       }
     }
   } else {

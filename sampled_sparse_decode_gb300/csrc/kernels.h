@@ -128,8 +128,8 @@ cudaError_t decode_launch_bf16_wide(const DecodeParams& p, int head_dim, int gro
 int decode_resident_bf16_wide(int head_dim, int group);
 int decode_max_clusters_bf16_wide(int head_dim, int group, int cluster);
 // compact path (bf16 decode steps with i.i.d. Horvitz-Thompson draws, no mixture, one
-// cluster per unit, every team sampled in each CTA): launchers of both variants and the
-// shape test; same shared memory and resident CTAs as the general kernel of each variant
+// cluster per unit, every team sampled in each CTA): launchers of both variants, the shape
+// test and the resident CTAs per SM (the plan is made for the general kernel's)
 cudaError_t decode_launch_bf16_fast(const DecodeParams& p, int head_dim, int group, dim3 grid,
                                     int cluster, cudaStream_t stream);
 cudaError_t decode_launch_bf16_wide_fast(const DecodeParams& p, int head_dim, int group,
@@ -138,6 +138,8 @@ bool decode_fast_fits_bf16(int head_dim, int group, int max_teams, int cluster, 
                            int num_draws);
 bool decode_fast_fits_bf16_wide(int head_dim, int group, int max_teams, int cluster,
                                 int team_size, int num_draws);
+int decode_resident_bf16_fast(int head_dim, int group);
+int decode_resident_bf16_wide_fast(int head_dim, int group);
 
 // Every host-side check santa_decode makes on `a`, then its launch plan; launches nothing
 // and touches no device memory.  On SANTA_OK *clusters_per_unit receives the plan's NC (> 1:

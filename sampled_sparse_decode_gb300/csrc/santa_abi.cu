@@ -126,6 +126,19 @@ int resident_ctas(bool bf16, int d, int G, bool wide) {
   return c;
 }
 
+// CTAs of the compact form of the bf16 kernel one SM holds (cached per device and shape).
+int compact_resident(int d, int G, bool wide) {
+  static std::mutex mu;
+  static int cache[64][2][2][santa::kMaxGroup + 1] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = cache[dev][wide][d == 128][G];
+  if (!c)
+    c = wide ? santa::decode_resident_bf16_wide_fast(d, G) : santa::decode_resident_bf16_fast(d, G);
+  return c;
+}
+
 // Clusters of `cl` CTAs the device can run at once (cached per device and shape).
 int max_clusters(bool bf16, int d, int G, int cl, bool wide) {
   static std::mutex mu;
@@ -216,12 +229,8 @@ int choose_variant(int dtype, int64_t units, int G, int d, int T, int max_teams,
   const int64_t sms = current_sms();
   if (units * pl->cluster * pl->clusters > sms) return SANTA_OK;
   Plan w;
-  // a sampling step scores ceil(max_teams / CL) teams per CTA before any K/V arrives: it
-  // keeps the larger cluster when the wide variant's would leave a CTA more than 64 teams
   if (choose(dtype, units, G, d, T, max_teams, M, mode, nc_cap, true, &w) == SANTA_OK &&
-      units * w.cluster * w.clusters <= sms &&
-      (mode != santa::kModeDecode || w.cluster >= pl->cluster ||
-       ceil_div(max_teams, w.cluster) <= 64))
+      units * w.cluster * w.clusters <= sms)
     *pl = w;
   return SANTA_OK;
 }
@@ -305,10 +314,14 @@ bool uses_compact_path(const santa_decode_args* a, int mode, const Plan& pl) {
   if (mode != santa::kModeDecode || a->dtype != SANTA_BF16 || pl.clusters != 1) return false;
   if (a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f) return false;
   const int G = a->num_q_heads / a->num_kv_heads;
-  return pl.wide ? santa::decode_fast_fits_bf16_wide(a->head_dim, G, a->max_teams, pl.cluster,
-                                                     a->team_size, a->num_draws)
-                 : santa::decode_fast_fits_bf16(a->head_dim, G, a->max_teams, pl.cluster,
-                                                a->team_size, a->num_draws);
+  const bool fits =
+      pl.wide ? santa::decode_fast_fits_bf16_wide(a->head_dim, G, a->max_teams, pl.cluster,
+                                                  a->team_size, a->num_draws)
+              : santa::decode_fast_fits_bf16(a->head_dim, G, a->max_teams, pl.cluster,
+                                             a->team_size, a->num_draws);
+  // the plan assumes the general kernel's resident CTAs per SM: the compact one must match
+  return fits &&
+         compact_resident(a->head_dim, G, pl.wide) >= resident_ctas(true, a->head_dim, G, pl.wide);
 }
 
 // Every host-side check of a call in `mode`, then its plan; launches nothing.
