@@ -150,6 +150,31 @@ __device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, ui
       : "memory");
 }
 
+// Stores to another CTA of the cluster that complete their bytes on that CTA's mbarrier:
+// dst and bar are cluster addresses (cluster_addr); dst 16- (v4) or 8-byte (v2) aligned.
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_v2(uint32_t dst, float a, float b, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];"
+      ::"r"(dst), "f"(a), "f"(b), "r"(bar)
+      : "memory");
+}
+
+// Atomic add at GPU scope with acquire-release semantics: the caller's earlier writes (and
+// those of its CTA, after a CTA barrier) are visible to whoever reads the sum later, and the
+// writes of the earlier adders are visible to the caller afterwards.
+__device__ __forceinline__ unsigned int atomic_add_acq_rel_gpu(unsigned int* addr, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+               : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // Two-dimensional tensor copy global -> shared through a tensor map (TMA): the box at
 // (x, y) (x the innermost coordinate, in elements) lands at dst and completes on bar.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,

@@ -123,8 +123,9 @@ struct DecodeTraits {
   static constexpr size_t kPOff = kTableOff + sizeof(ChunkMeta) * kMaxChunksPerSplit;
   static constexpr size_t kAOff = kPOff + sizeof(float) * kWarps * 64;
   static constexpr size_t kBarOff = kAOff + sizeof(float) * kWarps * kMaxGroup;
-  // mbarriers: one per stage, then two of the compact path (staged rows, score exchange)
-  static constexpr size_t kSmem = kBarOff + sizeof(uint64_t) * (kStages + 2);
+  // mbarriers: one per stage, then three of the compact path (staged rows, score exchange,
+  // the partials of the combine)
+  static constexpr size_t kSmem = kBarOff + sizeof(uint64_t) * (kStages + 3);
   static constexpr int kMinBlocks = (!W && kSmem <= 112 * 1024) ? 2 : 1;
   static_assert(!W || (BF16 && kStages % 2 == 0), "wide: bf16 only, even stage count");
 
@@ -511,6 +512,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         for (int s2 = 0; s2 < S; ++s2) mbar_init(&bar[s2], 1);
         mbar_init(rbar, Tr::kThreads);
         mbar_init(xbar, 1);
+        mbar_init(&bar[S + 2], 1);     // the combine's partials
         fence_mbar_init();
         s_abort = 0;
       }
@@ -1815,15 +1817,34 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       } else {
         v = reinterpret_cast<const float4*>(part)[qi];
       }
-      cluster.map_shared_rank(comb_q, r)[rank * qper + k] = v;
+      if constexpr (FAST)
+        st_async_v4(cluster_addr(smem_u32(comb_q + rank * qper + k), r), v,
+                    cluster_addr(smem_u32(&bar[S + 2]), r));
+      else
+        cluster.map_shared_rank(comb_q, r)[rank * qper + k] = v;
     }
     if (tid < CL * G) {
       const int r = tid / G, g = tid - r * G;
-      float* dst = cluster.map_shared_rank(comb_ml, r) + (rank * G + g) * 2;
-      dst[0] = part_m[g];
-      dst[1] = part_l[g];
+      if constexpr (FAST) {
+        st_async_v2(cluster_addr(smem_u32(comb_ml + (rank * G + g) * 2), r), part_m[g], part_l[g],
+                    cluster_addr(smem_u32(&bar[S + 2]), r));
+      } else {
+        float* dst = cluster.map_shared_rank(comb_ml, r) + (rank * G + g) * 2;
+        dst[0] = part_m[g];
+        dst[1] = part_l[g];
+      }
     }
-    cluster.sync();                                                 // barrier D1: delivered
+    if constexpr (FAST) {
+      // this CTA's slice of every peer's partial (and their (m, l)) has arrived: the bytes
+      // counted on its mbarrier, no cluster-wide barrier
+      if (tid == 0) {
+        const int nq_own = min(min(rank * qper, kQuads) + qper, kQuads) - min(rank * qper, kQuads);
+        mbar_arrive_expect_tx(&bar[S + 2], static_cast<uint32_t>(CL * (nq_own * 16 + G * 8)));
+      }
+      if (!mbar_wait(&bar[S + 2], 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
+    } else {
+      cluster.sync();                                               // barrier D1: delivered
+    }
   }
   float* out_unit = p.out + (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D;
   if (attending) {
@@ -1872,17 +1893,30 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   }
   if (!attending || NC == 1) return;
 
-  // ---- several clusters per unit: the last CTA to arrive merges the cluster partials
-  __threadfence();
+  // ---- several clusters per unit: the last CTA to arrive merges the cluster partials (its
+  // arrival ticket releases this CTA's partial writes and acquires everyone's)
   __syncthreads();
   if (tid == 0)
-    s_last = atomicAdd(&p.counters[unit], 1u) == static_cast<unsigned>(CL * NC - 1);
+    s_last = atomic_add_acq_rel_gpu(&p.counters[unit], 1u) == static_cast<unsigned>(CL * NC - 1);
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
+  // every load of this CTA at once (one round trip): thread t's quad of every cluster partial
+  // (G * d / 4 <= 256 quads) and, for t < NC * G, one cluster's (m, l) of one head
+  static_assert(G * D / 4 <= 256, "one output quad per thread");
+  const int qi = tid, gq = (qi * 4) / D;
+  float4 v[kMaxClustersPerUnit];
+  {
+    const float4* src =
+        reinterpret_cast<const float4*>(p.part_acc + static_cast<int64_t>(unit) * NC * G * D) + qi;
+#pragma unroll
+    for (int c = 0; c < kMaxClustersPerUnit; ++c)
+      v[c] = (c < NC && qi < kQuads) ? __ldcg(src + c * (G * D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (tid < NC * G) {
-    s_pm[tid] = __ldcg(&p.part_ml[(static_cast<int64_t>(unit) * NC * G + tid) * 2]);
-    s_pz[tid] = __ldcg(&p.part_ml[(static_cast<int64_t>(unit) * NC * G + tid) * 2 + 1]);
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) +
+                             static_cast<int64_t>(unit) * NC * G + tid);
+    s_pm[tid] = ml.x;
+    s_pz[tid] = ml.y;
   }
   __syncthreads();
   if (tid < G) {
@@ -1898,19 +1932,17 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     s_gz[tid] = l;
   }
   __syncthreads();
-  for (int qi = tid; qi < kQuads; qi += Tr::kThreads) {
-    const int g = (qi * 4) / D;
+  if (qi < kQuads) {
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < NC; ++c) {
-      const float w = s_pm[c * G + g];
-      const float4 v = __ldcg(
-          reinterpret_cast<const float4*>(p.part_acc + (static_cast<int64_t>(unit) * NC + c) * G * D) + qi);
-      a.x = fmaf(w, v.x, a.x);
-      a.y = fmaf(w, v.y, a.y);
-      a.z = fmaf(w, v.z, a.z);
-      a.w = fmaf(w, v.w, a.w);
+#pragma unroll
+    for (int c = 0; c < kMaxClustersPerUnit; ++c) {
+      const float w = c < NC ? s_pm[c * G + gq] : 0.f;
+      a.x = fmaf(w, v[c].x, a.x);
+      a.y = fmaf(w, v[c].y, a.y);
+      a.z = fmaf(w, v[c].z, a.z);
+      a.w = fmaf(w, v[c].w, a.w);
     }
-    const float l = s_gz[g];
+    const float l = s_gz[gq];
     const float inv = l > 0.f ? 1.f / l : 0.f;
     reinterpret_cast<float4*>(out_unit)[qi] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
   }

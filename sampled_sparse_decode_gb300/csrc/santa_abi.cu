@@ -219,14 +219,48 @@ int choose(int dtype, int64_t units, int G, int d, int T, int max_teams, int M, 
   return SANTA_OK;
 }
 
+// A dense bf16 plan on the wide variant that fills the device: the largest units * CL * NC
+// CTAs, at most one per SM, that the device can co-schedule (larger clusters on ties).
+// Returns false if no such plan reaches three quarters of the SMs.
+bool dense_fill_plan(int64_t units, int G, int d, int T, int max_teams, int64_t nc_cap,
+                     Plan* pl) {
+  const int64_t sms = current_sms();
+  const int64_t cmax = chunks_max_of(T, max_teams, 1, santa::kModeDense);
+  int64_t best = 0;
+  for (int cl = santa::kMaxCluster; cl >= 1; cl >>= 1) {
+    int64_t nc = std::min<int64_t>({santa::kMaxClustersPerUnit, std::max<int64_t>(1, nc_cap),
+                                    sms / (units * cl)});
+    const int maxc = max_clusters(true, d, G, cl, true);
+    nc = std::min<int64_t>(nc, maxc / units);
+    if (nc < 1 || ceil_div(cmax, cl * nc) > santa::kMaxChunksPerSplit) continue;
+    if (units * cl * nc > best) {
+      best = units * cl * nc;
+      pl->cluster = cl;
+      pl->clusters = static_cast<int>(nc);
+      pl->tpc = static_cast<int>(std::max<int64_t>(1, ceil_div(max_teams, cl)));
+      pl->wide = true;
+    }
+  }
+  return best * 4 >= sms * 3;
+}
+
 // The two-CTA-per-SM plan, replaced by the wide variant's plan when the step is a bf16
 // attending one and both plans need no more CTAs than the device has SMs (each CTA then has
-// an SM to itself anyway, and the wide variant consumes two chunks at a time).
+// an SM to itself anyway, and the wide variant consumes two chunks at a time).  A dense step
+// whose two-CTA-per-SM grid is under one and a half waves of SMs instead fills the device
+// with the wide variant (dense_fill_plan): uneven pairs of CTAs per SM set its tail.
 int choose_variant(int dtype, int64_t units, int G, int d, int T, int max_teams, int M,
                    int mode, int64_t nc_cap, Plan* pl) {
   int rc = choose(dtype, units, G, d, T, max_teams, M, mode, nc_cap, false, pl);
   if (rc || dtype != SANTA_BF16 || mode == santa::kModeSample) return rc;
   const int64_t sms = current_sms();
+  if (mode == santa::kModeDense) {
+    Plan w;
+    if (2 * units * pl->cluster * pl->clusters < 3 * sms &&
+        dense_fill_plan(units, G, d, T, max_teams, nc_cap, &w))
+      *pl = w;
+    return SANTA_OK;
+  }
   if (units * pl->cluster * pl->clusters > sms) return SANTA_OK;
   Plan w;
   if (choose(dtype, units, G, d, T, max_teams, M, mode, nc_cap, true, &w) == SANTA_OK &&
