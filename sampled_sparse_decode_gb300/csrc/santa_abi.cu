@@ -261,7 +261,17 @@ int choose_variant(int dtype, int64_t units, int G, int d, int T, int max_teams,
       *pl = w;
     return SANTA_OK;
   }
-  if (units * pl->cluster * pl->clusters > sms) return SANTA_OK;
+  if (units * pl->cluster * pl->clusters > sms) {
+    // a decode step whose units still get clusters of at least 4 CTAs with one CTA per SM
+    // takes the wide variant (more stages per SM; at Qwen B=8: 4 x 32 CTAs instead of 8 x 32
+    // two per SM, 0.4 us faster); smaller clusters stay on the two-CTA-per-SM variant
+    Plan w;
+    if (mode == santa::kModeDecode &&
+        choose(dtype, units, G, d, T, max_teams, M, mode, nc_cap, true, &w) == SANTA_OK &&
+        w.cluster >= 4 && units * w.cluster * w.clusters <= sms)
+      *pl = w;
+    return SANTA_OK;
+  }
   Plan w;
   if (choose(dtype, units, G, d, T, max_teams, M, mode, nc_cap, true, &w) == SANTA_OK &&
       units * w.cluster * w.clusters <= sms)
