@@ -108,8 +108,11 @@ struct DecodeTraits {
   static_assert(rep_rows(kMaxTeamsPerCta) >= 16, "representative buffer must hold 16 rows");
   static_assert(sizeof(ListEntry) * kMaxTeamsPerCta >= sizeof(float) * kPubScores,
                 "the list region must hold the published scores");
-  // phase D: warp merge buffer [8][G][D] + m, l [8][8], then the CTA partial [G][D] + m, l
-  static constexpr int kMergeFloats = kWarps * G * D + 2 * kWarps * kMaxGroup;
+  // phase D: warp merge buffer [8][G][D + 4] + m, l [8][8], then the CTA partial [G][D] + m, l.
+  // The 4-float pad puts the rows of heads g and g + 2 four banks apart: a warp's store of its
+  // mma accumulator fragment (8 rows of d x 4 heads per instruction) then hits 32 banks.
+  static constexpr int kMrgStride = D + 4;
+  static constexpr int kMergeFloats = kWarps * G * kMrgStride + 2 * kWarps * kMaxGroup;
   static constexpr int kPartialOff = kMergeFloats;                    // in floats
   static constexpr int kPartialFloats = G * D + 2 * kMaxGroup;
   static_assert((kMergeFloats + kPartialFloats) * 4 <= kRing, "merge buffers must fit");
@@ -1296,8 +1299,9 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   auto issue = [&](int ci) { issue_meta(ci, table[ci]); };
   if (tid >= early_n && tid < min(S, n_chunks)) issue(tid);   // chunks < early_n are out
 
-  float* mrg_acc = reinterpret_cast<float*>(smem);                   // [8][G][D]
-  float* mrg_m = mrg_acc + Tr::kWarps * G * D;                       // [8][8]
+  constexpr int kMS = Tr::kMrgStride;
+  float* mrg_acc = reinterpret_cast<float*>(smem);                   // [8][G][kMS]
+  float* mrg_m = mrg_acc + Tr::kWarps * G * kMS;                     // [8][8]
   float* mrg_l = mrg_m + Tr::kWarps * kMaxGroup;                     // [8][8]
   float* part = reinterpret_cast<float*>(smem) + Tr::kPartialOff;    // acc [G][D], m [8], l [8]
   float* part_m = part + G * D;
@@ -1438,7 +1442,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         for (int j = 0; j < 4; ++j) {
           const int d = 16 * t + (lane >> 2) + ((j >> 1) << 3);
           const int g = h0 + (j & 1);
-          if (g < G) mrg_acc[(warp * G + g) * D + d] = o[t][j];
+          if (g < G) mrg_acc[(warp * G + g) * kMS + d] = o[t][j];
         }
       if (lane < 4) {
         mrg_m[warp * kMaxGroup + h0] = mr0;
@@ -1607,7 +1611,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         for (int j = 0; j < 4; ++j) {
           const int d = dh * (D / 2) + 16 * t + (lane >> 2) + ((j >> 1) << 3);
           const int g = h0 + (j & 1);
-          if (g < G) mrg_acc[(warp * G + g) * D + d] = o[t][j];
+          if (g < G) mrg_acc[(warp * G + g) * kMS + d] = o[t][j];
         }
       if (lane < 4) {
         mrg_m[warp * kMaxGroup + h0] = mr0;
@@ -1751,7 +1755,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int e = 0; e < Tr::kEplV; ++e)
-          mrg_acc[(warp * G + g) * D + lane * Tr::kEplV + e] = acc[g][e];
+          mrg_acc[(warp * G + g) * kMS + lane * Tr::kEplV + e] = acc[g][e];
       if (!(lane & 0x11)) {
         mrg_m[warp * kMaxGroup + hh] = m_run;
         mrg_l[warp * kMaxGroup + hh] = l_run;
@@ -1779,7 +1783,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
 #pragma unroll
         for (int w = 0; w < Tr::kWarps; ++w) {
           const float mw = mrg_m[w * kMaxGroup + g];
-          a = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_acc[(w * G + g) * D + k], a);
+          a = fmaf(mw == kNegInf ? 0.f : exp2f(mw - mx), mrg_acc[(w * G + g) * kMS + k], a);
         }
         part[i] = a;
       }
@@ -1808,7 +1812,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
 #pragma unroll
         for (int w = 0; w < kW; ++w) {
           const float a = arow[w * kMaxGroup + g];
-          const float4 x = *reinterpret_cast<const float4*>(mrg_acc + ((w0 + w) * G + g) * D + k0);
+          const float4 x = *reinterpret_cast<const float4*>(mrg_acc + ((w0 + w) * G + g) * kMS + k0);
           v.x = fmaf(a, x.x, v.x);
           v.y = fmaf(a, x.y, v.y);
           v.z = fmaf(a, x.z, v.z);
