@@ -133,17 +133,18 @@ struct DecodeTraits {
   static_assert(!W || (BF16 && kStages % 2 == 0), "wide: bf16 only, even stage count");
 
   // Compact path (a decode step with i.i.d. Horvitz-Thompson draws, no mixture, one cluster
-  // per unit).  CTA r scores the slice of `fast_per` teams starting at r * fast_per (a
-  // multiple of 4, so each slice is a whole number of 16-byte pieces) and sends its G + 1
-  // rows (the G heads' scores, then the page ids) from its list region to every CTA, row g
-  // into row g of the receive buffer [G + 1][cluster * fast_per] at the end of the ring, so
-  // that each row holds every team of the unit in team order.  In front of it, from the
-  // first stage the scratch needs: the CDF [cap] uint64, drawn flags and p (then pi) [cap]
-  // 4 B each.  The representative rows are staged from the start of the ring up to the
-  // receive buffer (peers may send while this CTA still scores; everything else is written
-  // after).
+  // per unit).  CTA r scores the slice of `fast_per` teams starting at r * fast_per (a power
+  // of two >= 4, so each slice is a whole number of 16-byte pieces and team j's rank and
+  // place in it are shifts) and sends its block [G + 1][fast_per] (the G heads' scores, then
+  // the page ids) from its list region to every CTA, into block r of the receive buffer
+  // [cluster][G + 1][fast_per] at the end of the ring.  In front of it, from the first stage
+  // the scratch needs: the CDF [cap] uint64, drawn flags and p (then pi) [cap] 4 B each.
+  // The representative rows are staged from the start of the ring up to the receive buffer
+  // (peers may send while this CTA still scores; everything else is written after).
   static constexpr int fast_per(int max_teams, int cluster) {
-    return ((max_teams + cluster - 1) / cluster + 3) / 4 * 4;
+    int per = 4;
+    while (per < (max_teams + cluster - 1) / cluster) per *= 2;
+    return per;
   }
   static constexpr size_t fast_recv_bytes(int max_teams, int cluster) {
     return (G + 1) * static_cast<size_t>(cluster) * fast_per(max_teams, cluster) * 4;
@@ -490,12 +491,16 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     // code runs once per launch, so it is kept short (rolled loops) and has few phases: the
     // SM waits on fetching straight-line instructions here more than on the arithmetic.
     const int n_max = p.max_teams;
-    const int per = Tr::fast_per(n_max, CL);           // teams scored per CTA, multiple of 4
+    const int per = Tr::fast_per(n_max, CL);           // teams scored per CTA, power of 2
     const int lo = rank * per;
     const int nl = max(0, min(per, n_max - lo));
     const int cap = (n_max + 3) & ~3;
     early_n = S - Tr::fast_scratch_stages(n_max, CL);     // stages in front of the scratch
-    const int RL = CL * per;                           // row length of the receive buffer
+    const int RS = (G + 1) * per;                      // floats of one rank's block
+    const int lp = __ffs(per) - 1;
+    // team j's entry of row g (g = G: its page id) in the receive buffer: block j >> lp,
+    // place j & (per - 1)
+    auto at = [&](int j, int g) { return j + (((j >> lp) * G + g) << lp); };
     float* xs = reinterpret_cast<float*>(smem + Tr::kRing - Tr::fast_recv_bytes(n_max, CL));
     unsigned long long* cdf = reinterpret_cast<unsigned long long*>(
         smem + static_cast<size_t>(early_n) * Tr::kStageBytes);        // [cap]
@@ -503,7 +508,6 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     float* ps = reinterpret_cast<float*>(flg + cap);                     // [cap] p
     float* rows = reinterpret_cast<float*>(smem);      // [per][D] staged representatives
     float* mine = reinterpret_cast<float*>(list);      // [G + 1][per] this CTA's slice, sent
-    int* pg = reinterpret_cast<int*>(xs + G * RL);       // [RL] page id of every team
     uint64_t* rbar = &bar[S];                          // staged rows
     uint64_t* xbar = &bar[S + 1];                      // the received slices
     const bool bad_layout = BF16 && (smem_u32(smem) & 1023u) != 0;
@@ -520,7 +524,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         s_abort = 0;
       }
       __syncthreads();                // the mbarriers are initialised
-      if (tid == 0) mbar_arrive_expect_tx(xbar, static_cast<uint32_t>((G + 1) * RL * 4));
+      if (tid == 0) mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(CL * RS * 4));
       cluster_arrive_relaxed();       // split barrier: this CTA runs, its mbarriers are set up
     }
     grid_dependency_wait();
@@ -567,8 +571,9 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         }
     }
     if (!mbar_wait(rbar, 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
-    // ---- the slice's scores s_{g,j} = q_g . rep_j / sqrt(d): 16 lanes per team, lane l ends
-    // with head (l >> 1) & 7; -inf past the sequence and for bad page ids
+    // ---- the slice's scores s_{g,j} = q_g . rep_j / sqrt(d), kept in base 2 (times log2 e,
+    // so that exp(s - m) is one exp2): 16 lanes per team, lane l ends with head (l >> 1) & 7;
+    // -inf past the sequence and for bad page ids
     {
       const int hh = (lane >> 1) & 7;
 #pragma unroll 2
@@ -594,19 +599,27 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         const float sum = reduce_scatter8(part, lane);
         if (jl < nl && !(lane & 1) && hh < G) {
           const bool ok = __float_as_int(mine[G * per + jl]) >= 0 && lo + jl < n;
-          mine[hh * per + jl] = ok ? sum * p.scale : kNegInf;
+          mine[hh * per + jl] = ok ? sum * p.scale_log2 : kNegInf;   // base 2
         }
       }
     }
-    // ---- send the slice to every CTA of the cluster (itself included): row g of it to
-    // row g of the receiver's buffer, one bulk copy each, completing on the receiver's xbar
+    // ---- send the slice to every CTA of the cluster (itself included), into block `rank`
+    // of the receiver's buffer: bulk copies of at most 2 KB (more copies in flight, few to
+    // issue), completing on the receiver's xbar
     fence_proxy_async_smem();         // slice written, staged rows read: both by the async proxy next
     __syncthreads();
     cluster_wait();                   // every peer runs and has initialised its mbarriers
-    if (tid < (G + 1) * CL) {
-      const int row = tid / CL, dst = tid - row * CL;
-      bulk_s2cluster(cluster_addr(smem_u32(xs + row * RL + rank * per), dst), mine + row * per,
-                     static_cast<uint32_t>(per * 4), cluster_addr(smem_u32(xbar), dst));
+    {
+      constexpr int kPiece = 2048;
+      const int bytes = RS * 4, npc = (bytes + kPiece - 1) / kPiece;
+#pragma unroll 1
+      for (int i = tid; i < CL * npc; i += Tr::kThreads) {
+        const int dst = i / npc, off = (i - dst * npc) * kPiece;
+        bulk_s2cluster(cluster_addr(smem_u32(xs + rank * RS) + off, dst),
+                       reinterpret_cast<unsigned char*>(mine) + off,
+                       static_cast<uint32_t>(min(kPiece, bytes - off)),
+                       cluster_addr(smem_u32(xbar), dst));
+      }
     }
     // the Philox word of draw tid (it needs nothing else) while the slices arrive; kept in
     // shared memory so that it is computed here and not next to its use
@@ -618,21 +631,20 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
                                                    static_cast<uint32_t>(h),
                                                    static_cast<uint32_t>(b), 0u), key).x;
     if (!mbar_wait(xbar, 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
-    // ---- per-head statistics over the unit, warp g on row g: m_g, e_gj = exp(s_gj - m_g) in
-    // place and 1 / (G z_g); four independent teams per lane at a time, summed in a fixed
-    // order (the same in every CTA)
+    // ---- per-head statistics over the unit, warp g on row g: m_g, e_gj = exp(s_gj - m_g)
+    // (2^ of the base-2 scores) in place and 1 / (G z_g); four independent teams per lane at a
+    // time, summed in a fixed order (the same in every CTA)
     const bool out_writer = rank == 0;
     const int tpt = (n_max + Tr::kThreads - 1) / Tr::kThreads;
     const int jt = tid * tpt;
     __shared__ float s_zinv[kMaxGroup];
     if (warp < G) {
-      float* row = xs + warp * RL;
       float m = kNegInf;
 #pragma unroll 1
       for (int j0 = lane; j0 < n_max; j0 += 128) {
         float v[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = j0 + 32 * k < n_max ? row[j0 + 32 * k] : kNegInf;
+        for (int k = 0; k < 4; ++k) v[k] = j0 + 32 * k < n_max ? xs[at(j0 + 32 * k, warp)] : kNegInf;
         m = fmaxf(m, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
       }
       m = warp_max(m);
@@ -643,9 +655,10 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         for (int k = 0; k < 4; ++k) {
           const int j = j0 + 32 * k;
           if (j < n_max) {
-            const float sv = row[j];
-            const float ev = sv == kNegInf ? 0.f : expf(sv - m);
-            row[j] = ev;
+            const int a = at(j, warp);
+            const float sv = xs[a];
+            const float ev = sv == kNegInf ? 0.f : exp2f(sv - m);
+            xs[a] = ev;
             z += ev;
           }
         }
@@ -666,7 +679,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       if (j < n_max) {
         float pj = 0.f;
 #pragma unroll
-        for (int g = 0; g < G; ++g) pj = fmaf(xs[g * RL + j], zg[g], pj);
+        for (int g = 0; g < G; ++g) pj = fmaf(xs[at(j, g)], zg[g], pj);
         unsigned long long P = 0ull;
         if (pj > 0.f) {
           const float x = pj * 0x1p62f;                              // exact scaling
@@ -715,14 +728,14 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     }
     // pi_j = 1 - (1 - p_j)^M and the weight -log2 pi_j of every team, threads in reverse order
     // (those that drew nothing take the first teams): ps becomes pi, and the weight goes to
-    // the first score row of the received slices, no longer read
+    // the team's head-0 score in the receive buffer, no longer read
     {
       const float Mf = static_cast<float>(M);
 #pragma unroll 1
       for (int j = Tr::kThreads - 1 - tid; j < n_max; j += Tr::kThreads) {
         const float piv = -expm1f(Mf * log1pf(-ps[j]));
         ps[j] = piv;
-        xs[j] = -log2f(piv);
+        xs[at(j, 0)] = -log2f(piv);
       }
     }
     __syncthreads();
@@ -749,7 +762,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
             p.sel_ids[static_cast<int64_t>(unit) * M + k] = j;
             p.pi[static_cast<int64_t>(unit) * M + k] = ps[j];
           }
-          const int page = pg[j];
+          const int page = __float_as_int(xs[at(j, G)]);
           const bool pok = page >= 0 && page < p.num_pages;
 #pragma unroll 1
           for (int part = 0; part < cpt; ++part) {
@@ -758,7 +771,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
               const int vt = pok ? max(0, min(min(p.team_size, L - j * p.team_size) -
                                                   part * kChunk, kChunk))
                                  : 0;
-              const ChunkMeta m{vt > 0 ? page : -1, vt, xs[j], part};
+              const ChunkMeta m{vt > 0 ? page : -1, vt, xs[at(j, 0)], part};
               table[ci] = m;
               if (ci < early_n) issue_meta(ci, m);
             }
