@@ -257,6 +257,14 @@ inline cudaError_t ensure_dynamic_smem(Kernel* kernel, size_t bytes,
   return e;
 }
 
+// 2^x by the SFU's approximate instruction (relative error near 2^-22; results below 2^-126
+// flush to zero, 2^-inf is 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- warp reductions
 
 __device__ __forceinline__ float warp_sum(float v) {

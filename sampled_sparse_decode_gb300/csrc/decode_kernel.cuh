@@ -651,16 +651,18 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       float z = 0.f;
 #pragma unroll 1
       for (int j0 = lane; j0 < n_max; j0 += 128) {
+        int a[4];
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {          // every load of the four before any store
+          a[k] = at(j0 + 32 * k, warp);
+          v[k] = j0 + 32 * k < n_max ? xs[a[k]] : kNegInf;
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int j = j0 + 32 * k;
-          if (j < n_max) {
-            const int a = at(j, warp);
-            const float sv = xs[a];
-            const float ev = sv == kNegInf ? 0.f : exp2f(sv - m);
-            xs[a] = ev;
-            z += ev;
-          }
+          const float ev = v[k] == kNegInf ? 0.f : ex2_approx(v[k] - m);
+          if (j0 + 32 * k < n_max) xs[a[k]] = ev;
+          z += ev;
         }
       }
       z = warp_sum(z);
@@ -1391,12 +1393,12 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
       const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
-      const float al0 = mn0 == kNegInf ? 1.f : exp2f(mr0 - mn0);
-      const float al1 = mn1 == kNegInf ? 1.f : exp2f(mr1 - mn1);
-      const float p0 = mn0 == kNegInf ? 0.f : exp2f(s0 - mn0);
-      const float p1 = mn1 == kNegInf ? 0.f : exp2f(s1 - mn1);
-      const float p2 = mn0 == kNegInf ? 0.f : exp2f(s2 - mn0);
-      const float p3 = mn1 == kNegInf ? 0.f : exp2f(s3 - mn1);
+      const float al0 = mn0 == kNegInf ? 1.f : ex2_approx(mr0 - mn0);
+      const float al1 = mn1 == kNegInf ? 1.f : ex2_approx(mr1 - mn1);
+      const float p0 = mn0 == kNegInf ? 0.f : ex2_approx(s0 - mn0);
+      const float p1 = mn1 == kNegInf ? 0.f : ex2_approx(s1 - mn1);
+      const float p2 = mn0 == kNegInf ? 0.f : ex2_approx(s2 - mn0);
+      const float p3 = mn1 == kNegInf ? 0.f : ex2_approx(s3 - mn1);
       lr0 = fmaf(lr0, al0, p0 + p2);
       lr1 = fmaf(lr1, al1, p1 + p3);
       mr0 = mn0;
@@ -1563,12 +1565,12 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
       const float mn0 = fmaxf(mr0, mx0), mn1 = fmaxf(mr1, mx1);
-      const float al0 = mn0 == kNegInf ? 1.f : exp2f(mr0 - mn0);
-      const float al1 = mn1 == kNegInf ? 1.f : exp2f(mr1 - mn1);
-      const float p0 = mn0 == kNegInf ? 0.f : exp2f(s0 - mn0);
-      const float p1 = mn1 == kNegInf ? 0.f : exp2f(s1 - mn1);
-      const float p2 = mn0 == kNegInf ? 0.f : exp2f(s2 - mn0);
-      const float p3 = mn1 == kNegInf ? 0.f : exp2f(s3 - mn1);
+      const float al0 = mn0 == kNegInf ? 1.f : ex2_approx(mr0 - mn0);
+      const float al1 = mn1 == kNegInf ? 1.f : ex2_approx(mr1 - mn1);
+      const float p0 = mn0 == kNegInf ? 0.f : ex2_approx(s0 - mn0);
+      const float p1 = mn1 == kNegInf ? 0.f : ex2_approx(s1 - mn1);
+      const float p2 = mn0 == kNegInf ? 0.f : ex2_approx(s2 - mn0);
+      const float p3 = mn1 == kNegInf ? 0.f : ex2_approx(s3 - mn1);
       lr0 = fmaf(lr0, al0, p0 + p2);
       lr1 = fmaf(lr1, al1, p1 + p3);
       mr0 = mn0;
