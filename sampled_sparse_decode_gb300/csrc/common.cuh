@@ -139,17 +139,6 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t smem_addr, int rank) {
   return r;
 }
 
-// One contiguous bulk copy from this CTA's shared memory into another CTA's of the cluster
-// (TMA), completing `bytes` transaction bytes on the destination CTA's mbarrier; dst and
-// bar are cluster addresses (cluster_addr), src a local one.  All multiples of 16 bytes.
-__device__ __forceinline__ void bulk_s2cluster(uint32_t dst, const void* src, uint32_t bytes,
-                                               uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // Stores to another CTA of the cluster that complete their bytes on that CTA's mbarrier:
 // dst and bar are cluster addresses (cluster_addr); dst 16- (v4) or 8-byte (v2) aligned.
 __device__ __forceinline__ void st_async_v4(uint32_t dst, float4 v, uint32_t bar) {

@@ -42,6 +42,16 @@
 //            cluster barrier each CTA merges its slice in rank order.  With NC > 1 the
 //            cluster partials go to global scratch and the last CTA of the unit (an atomic
 //            ticket, no waiting) merges them in cluster order.
+// Compact form (template flag FAST: a bf16 decode step with i.i.d. Horvitz-Thompson draws,
+// no mixture, NC = 1).  Phases A and B are replaced by a shorter sequence: CTA r stages its
+// slice's representative rows by one bulk copy each, scores them in base 2, and stores its
+// [G + 1][slice] block (scores, page ids) into every CTA with st.async, completing on the
+// receiver's mbarrier (no cluster barrier); each CTA then takes the per-head statistics
+// (warp per head), p and the CDF (one block scan), the draws (binary search, Philox words
+// computed while the rows were in flight), pi for every team, and writes S with the chunk
+// table in one pass, issuing the first copies at once.  In phase D the partial quads go by
+// st.async to the owner's mbarrier, and each CTA waits only for its own slice.  Its code is
+// kept short: it runs once per launch, and the SM waits on fetching cold instructions there.
 // The kernel is launched with programmatic stream serialization and touches global memory
 // only after griddepcontrol.wait.  No wait is unbounded: mbarrier waits give up after 2 s
 // (status bit, clean exit through the remaining barriers); every CTA executes every cluster
@@ -511,6 +521,9 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     uint64_t* rbar = &bar[S];                          // staged rows
     uint64_t* xbar = &bar[S + 1];                      // the received slices
     const bool bad_layout = BF16 && (smem_u32(smem) & 1023u) != 0;
+    __shared__ uint32_t s_xw[Tr::kThreads];
+    const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
+                                 static_cast<uint32_t>(p.seed >> 32));
     if (!bad_layout) {
       // shared memory only: allowed before the previous kernel of the stream has finished
       if (tid == 0) {
@@ -570,6 +583,16 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
           qs[g][4 * e4 + 3] = bf16_hi(w.y);
         }
     }
+    // the Philox word of each draw r < 256 (it needs only the seed and the unit) while the
+    // representative rows are in flight; draw r falls to thread (r mod 32) * 8 + r / 32, so
+    // the first draws spread over all warps
+    {
+      const int r = (tid & 7) * 32 + (tid >> 3);
+      if (r < M)
+        s_xw[r] = philox4x32_10_compact(make_uint4(static_cast<uint32_t>(r),
+                                                   static_cast<uint32_t>(h),
+                                                   static_cast<uint32_t>(b), 0u), key).x;
+    }
     if (!mbar_wait(rbar, 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
     // ---- the slice's scores s_{g,j} = q_g . rep_j / sqrt(d), kept in base 2 (times log2 e,
     // so that exp(s - m) is one exp2): 16 lanes per team, lane l ends with head (l >> 1) & 7;
@@ -604,32 +627,21 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       }
     }
     // ---- send the slice to every CTA of the cluster (itself included), into block `rank`
-    // of the receiver's buffer: bulk copies of at most 2 KB (more copies in flight, few to
-    // issue), completing on the receiver's xbar
-    fence_proxy_async_smem();         // slice written, staged rows read: both by the async proxy next
+    // of the receiver's buffer: 16-byte st.async stores from every thread, whose bytes
+    // complete on the receiver's xbar (bulk copies took the issuing threads longer)
+    fence_proxy_async_smem();         // staged rows read: the ring's start is refilled by copies later
     __syncthreads();
     cluster_wait();                   // every peer runs and has initialised its mbarriers
     {
-      constexpr int kPiece = 2048;
-      const int bytes = RS * 4, npc = (bytes + kPiece - 1) / kPiece;
+      const int nq = RS / 4;                           // 16-byte quads of one block
+      const float4* src = reinterpret_cast<const float4*>(mine);
 #pragma unroll 1
-      for (int i = tid; i < CL * npc; i += Tr::kThreads) {
-        const int dst = i / npc, off = (i - dst * npc) * kPiece;
-        bulk_s2cluster(cluster_addr(smem_u32(xs + rank * RS) + off, dst),
-                       reinterpret_cast<unsigned char*>(mine) + off,
-                       static_cast<uint32_t>(min(kPiece, bytes - off)),
-                       cluster_addr(smem_u32(xbar), dst));
+      for (int i = tid; i < CL * nq; i += Tr::kThreads) {
+        const int dst = i / nq, qd = i - dst * nq;
+        st_async_v4(cluster_addr(smem_u32(xs + rank * RS + 4 * qd), dst), src[qd],
+                    cluster_addr(smem_u32(xbar), dst));
       }
     }
-    // the Philox word of draw tid (it needs nothing else) while the slices arrive; kept in
-    // shared memory so that it is computed here and not next to its use
-    __shared__ uint32_t s_xw[Tr::kThreads];
-    const uint2 key = make_uint2(static_cast<uint32_t>(p.seed),
-                                 static_cast<uint32_t>(p.seed >> 32));
-    if (tid < M)
-      s_xw[tid] = philox4x32_10_compact(make_uint4(static_cast<uint32_t>(tid),
-                                                   static_cast<uint32_t>(h),
-                                                   static_cast<uint32_t>(b), 0u), key).x;
     if (!mbar_wait(xbar, 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
     // ---- per-head statistics over the unit, warp g on row g: m_g, e_gj = exp(s_gj - m_g)
     // (2^ of the base-2 scores) in place and 1 / (G z_g); four independent teams per lane at a
