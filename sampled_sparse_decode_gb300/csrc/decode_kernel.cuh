@@ -148,7 +148,7 @@ struct DecodeTraits {
   // place in it are shifts) and sends its block [G + 1][fast_per] (the G heads' scores, then
   // the page ids) from its list region to every CTA, into block r of the receive buffer
   // [cluster][G + 1][fast_per] at the end of the ring.  In front of it, from the first stage
-  // the scratch needs: the CDF [cap] uint64, drawn flags and p (then pi) [cap] 4 B each.
+  // the scratch needs: the CDF [cap] uint64, drawn flags and pi [cap] 4 B each.
   // The representative rows are staged from the start of the ring up to the receive buffer
   // (peers may send while this CTA still scores; everything else is written after).
   static constexpr int fast_per(int max_teams, int cluster) {
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     unsigned long long* cdf = reinterpret_cast<unsigned long long*>(
         smem + static_cast<size_t>(early_n) * Tr::kStageBytes);        // [cap]
     int* flg = reinterpret_cast<int*>(cdf + cap);                        // [cap] drawn
-    float* ps = reinterpret_cast<float*>(flg + cap);                     // [cap] p
+    float* ps = reinterpret_cast<float*>(flg + cap);                     // [cap] pi
     float* rows = reinterpret_cast<float*>(smem);      // [per][D] staged representatives
     float* mine = reinterpret_cast<float*>(list);      // [G + 1][per] this CTA's slice, sent
     uint64_t* rbar = &bar[S];                          // staged rows
@@ -703,7 +703,11 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         }
         run += P;
         cdf[j] = run;                 // this thread's inclusive sum; its prefix is added below
-        ps[j] = pj;
+        // pi_j = 1 - (1 - p_j)^M and the weight -log2 pi_j (to the team's head-0 entry of
+        // the receive buffer, no longer read); independent of the scan below
+        const float piv = -expm1f(static_cast<float>(M) * log1pf(-pj));
+        ps[j] = piv;
+        xs[at(j, 0)] = -log2f(piv);
         flg[j] = 0;
         if (p.team_probs && out_writer)
           p.team_probs[static_cast<int64_t>(unit) * p.max_teams + j] = pj;
@@ -739,18 +743,6 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     } else if (out_writer) {
 #pragma unroll 1
       for (int r = tid; r < M; r += Tr::kThreads) p.draw_ids[static_cast<int64_t>(unit) * M + r] = -1;
-    }
-    // pi_j = 1 - (1 - p_j)^M and the weight -log2 pi_j of every team, threads in reverse order
-    // (those that drew nothing take the first teams): ps becomes pi, and the weight goes to
-    // the team's head-0 score in the receive buffer, no longer read
-    {
-      const float Mf = static_cast<float>(M);
-#pragma unroll 1
-      for (int j = Tr::kThreads - 1 - tid; j < n_max; j += Tr::kThreads) {
-        const float piv = -expm1f(Mf * log1pf(-ps[j]));
-        ps[j] = piv;
-        xs[at(j, 0)] = -log2f(piv);
-      }
     }
     __syncthreads();
     // ---- S in ascending team order (per-thread counts, a block scan: slot k of each drawn
