@@ -1469,22 +1469,6 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         mrg_l[warp * kMaxGroup + h0] = lr0;
         mrg_l[warp * kMaxGroup + h0 + 1] = lr1;
       }
-      __syncthreads();
-      if (tid < G) {
-        float mx = kNegInf;
-#pragma unroll
-        for (int w = 0; w < Tr::kWarps; ++w) mx = fmaxf(mx, mrg_m[w * kMaxGroup + tid]);
-        float l = 0.f;
-#pragma unroll
-        for (int w = 0; w < Tr::kWarps; ++w) {
-          const float mw = mrg_m[w * kMaxGroup + tid];
-          const float wt = mw == kNegInf ? 0.f : exp2f(mw - mx);
-          arow[w * kMaxGroup + tid] = wt;
-          l = fmaf(wt, mrg_l[w * kMaxGroup + tid], l);
-        }
-        part_m[tid] = mx;
-        part_l[tid] = l;
-      }
       __syncthreads();      // the combine's push forms each partial quad from mrg_acc
     }
   } else if constexpr (BF16) {
@@ -1637,24 +1621,6 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         mrg_m[warp * kMaxGroup + h0 + 1] = mr1;
         mrg_l[warp * kMaxGroup + h0] = lr0;
         mrg_l[warp * kMaxGroup + h0 + 1] = lr1;
-      }
-      __syncthreads();
-      // CTA partial: the four token tiles of each half of d (both halves share m and l);
-      // the tile weights exp2(m_t - m) once per head
-      if (tid < G) {
-        float mx = kNegInf;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mrg_m[w * kMaxGroup + tid]);
-        float l = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float mw = mrg_m[w * kMaxGroup + tid];
-          const float wt = mw == kNegInf ? 0.f : exp2f(mw - mx);
-          arow[w * kMaxGroup + tid] = wt;
-          l = fmaf(wt, mrg_l[w * kMaxGroup + tid], l);
-        }
-        part_m[tid] = mx;
-        part_l[tid] = l;
       }
       __syncthreads();      // the combine's push forms each partial quad from mrg_acc
     }
@@ -1822,15 +1788,22 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       const int r = qi / qper, k = qi - r * qper;
       float4 v;
       if constexpr (BF16) {
-        // the CTA partial quad straight from the warp partials: weights arow[w][g] of
-        // every warp (wide) or of the four token tiles of this half of d
+        // the CTA partial quad straight from the warp partials, weighted exp2(m_w - m) over
+        // every warp (wide) or the four token tiles of this half of d (both halves share m
+        // and l, kept by warps 0-3), each thread forming its head's weights itself
         const int g = (4 * qi) / D, k0 = 4 * qi - g * D;
         constexpr int kW = W ? Tr::kWarps : 4;
         const int w0 = W ? 0 : (k0 / (D / 2)) * 4;
+        float mw[kW], mx = kNegInf;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {
+          mw[w] = mrg_m[w * kMaxGroup + g];
+          mx = fmaxf(mx, mw[w]);
+        }
         v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kW; ++w) {
-          const float a = arow[w * kMaxGroup + g];
+          const float a = mw[w] == kNegInf ? 0.f : ex2_approx(mw[w] - mx);
           const float4 x = *reinterpret_cast<const float4*>(mrg_acc + ((w0 + w) * G + g) * kMS + k0);
           v.x = fmaf(a, x.x, v.x);
           v.y = fmaf(a, x.y, v.y);
@@ -1848,13 +1821,30 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     }
     if (tid < CL * G) {
       const int r = tid / G, g = tid - r * G;
+      float pm, pl;
+      if constexpr (BF16) {
+        // the CTA's (m, l) of head g from the warps' (the same weights as above)
+        constexpr int kW = W ? Tr::kWarps : 4;
+        pm = kNegInf;
+        pl = 0.f;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) pm = fmaxf(pm, mrg_m[w * kMaxGroup + g]);
+#pragma unroll
+        for (int w = 0; w < kW; ++w) {
+          const float mw = mrg_m[w * kMaxGroup + g];
+          pl = fmaf(mw == kNegInf ? 0.f : ex2_approx(mw - pm), mrg_l[w * kMaxGroup + g], pl);
+        }
+      } else {
+        pm = part_m[g];
+        pl = part_l[g];
+      }
       if constexpr (FAST) {
-        st_async_v2(cluster_addr(smem_u32(comb_ml + (rank * G + g) * 2), r), part_m[g], part_l[g],
+        st_async_v2(cluster_addr(smem_u32(comb_ml + (rank * G + g) * 2), r), pm, pl,
                     cluster_addr(smem_u32(&bar[S + 2]), r));
       } else {
         float* dst = cluster.map_shared_rank(comb_ml, r) + (rank * G + g) * 2;
-        dst[0] = part_m[g];
-        dst[1] = part_l[g];
+        dst[0] = pm;
+        dst[1] = pl;
       }
     }
     if constexpr (FAST) {
@@ -1870,6 +1860,36 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     }
   }
   float* out_unit = p.out + (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D;
+  if (attending && FAST) {
+    // this CTA's slice of the output: each thread forms the CL ranks' weights of its quad's
+    // head itself and merges in rank order (no barrier)
+    const int q0 = min(rank * qper, kQuads);
+    const int nq = min(q0 + qper, kQuads) - q0;
+    for (int k = tid; k < nq; k += Tr::kThreads) {
+      const int qi = q0 + k;
+      const int g = (qi * 4) / D;
+      float mx = kNegInf;
+#pragma unroll 4
+      for (int r = 0; r < CL; ++r) mx = fmaxf(mx, comb_ml[(r * G + g) * 2]);
+      float l = 0.f;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int r = 0; r < CL; ++r) {
+        const float mr = comb_ml[(r * G + g) * 2];
+        const float w = mr == kNegInf ? 0.f : ex2_approx(mr - mx);
+        l = fmaf(w, comb_ml[(r * G + g) * 2 + 1], l);
+        const float4 v = comb_q[r * qper + k];
+        a.x = fmaf(w, v.x, a.x);
+        a.y = fmaf(w, v.y, a.y);
+        a.z = fmaf(w, v.z, a.z);
+        a.w = fmaf(w, v.w, a.w);
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      reinterpret_cast<float4*>(out_unit)[qi] =
+          make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+    }
+    return;
+  }
   if (attending) {
     // weights of the CL partials per head: warp g, lane r
     if (warp < G) {
