@@ -93,6 +93,11 @@ __global__ void __launch_bounds__(kRepThreads) reps_kernel(RepsParams p) {
   const int col = threadIdx.x % Sp::kCols;
   const int group = threadIdx.x / Sp::kCols;
   const int64_t items = static_cast<int64_t>(p.num_items) * p.num_kv_heads;
+  // launched as a programmatic dependent launch: global memory only after the previous
+  // kernel of the stream has completed; the next one may be scheduled from here on (it is
+  // launched once every block of this grid has passed this point, and waits in turn)
+  grid_dependency_wait();
+  grid_launch_dependents();
   for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
     const int h = static_cast<int>(item % p.num_kv_heads);
     const int64_t listed = item / p.num_kv_heads;
@@ -195,18 +200,22 @@ cudaError_t launch_reps(const RepsParams& p, int head_dim, cudaStream_t stream) 
   const int64_t items = static_cast<int64_t>(p.num_items) * p.num_kv_heads;
   if (items == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(items < (1ll << 30) ? items : (1ll << 30));
-  if (p.is_bf16) {
-    if (head_dim == 128)
-      reps_kernel<true, 128><<<grid, kRepThreads, 0, stream>>>(p);
-    else
-      reps_kernel<true, 64><<<grid, kRepThreads, 0, stream>>>(p);
-  } else {
-    if (head_dim == 128)
-      reps_kernel<false, 128><<<grid, kRepThreads, 0, stream>>>(p);
-    else
-      reps_kernel<false, 64><<<grid, kRepThreads, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  // programmatic stream serialization: the blocks of this launch may be scheduled while the
+  // previous kernel of the stream drains (they wait for it before touching memory)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRepThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.is_bf16)
+    return head_dim == 128 ? cudaLaunchKernelEx(&cfg, reps_kernel<true, 128>, p)
+                           : cudaLaunchKernelEx(&cfg, reps_kernel<true, 64>, p);
+  return head_dim == 128 ? cudaLaunchKernelEx(&cfg, reps_kernel<false, 128>, p)
+                         : cudaLaunchKernelEx(&cfg, reps_kernel<false, 64>, p);
 }
 
 }  // namespace santa
