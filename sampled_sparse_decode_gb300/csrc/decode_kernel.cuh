@@ -38,10 +38,10 @@
 //            W = true (launches that fit one CTA per SM): six stages, two warp groups
 //            consuming alternate chunks on their own stages.
 //   phase D  the warps merge into a CTA partial; each CTA pushes the quads of the output
-//            slice rank r owns, with its (m, l), into rank r's shared memory; after one
-//            cluster barrier each CTA merges its slice in rank order.  With NC > 1 the
-//            cluster partials go to global scratch and the last CTA of the unit (an atomic
-//            ticket, no waiting) merges them in cluster order.
+//            slice rank r owns, with its (m, l), into rank r's shared memory (st.async,
+//            completing on rank r's mbarrier); each CTA merges its slice in rank order.
+//            With NC > 1 the cluster partials go to global scratch and the last CTA of the
+//            unit (an atomic ticket, no waiting) merges them in cluster order.
 // Compact form (template flag FAST: a bf16 decode step with i.i.d. Horvitz-Thompson draws,
 // no mixture, NC = 1).  Phases A and B are replaced by a shorter sequence: CTA r stages its
 // slice's representative rows by one bulk copy each, scores them in base 2, and stores its
@@ -49,9 +49,9 @@
 // receiver's mbarrier (no cluster barrier); each CTA then takes the per-head statistics
 // (warp per head), p and the CDF (one block scan), the draws (binary search, Philox words
 // computed while the rows were in flight), pi for every team, and writes S with the chunk
-// table in one pass, issuing the first copies at once.  In phase D the partial quads go by
-// st.async to the owner's mbarrier, and each CTA waits only for its own slice.  Its code is
-// kept short: it runs once per launch, and the SM waits on fetching cold instructions there.
+// table in one pass, issuing the first copies at once.  In phase D each merging thread forms
+// its head's weights itself.  Its code is kept short: it runs once per launch, and the SM
+// waits on fetching cold instructions there.
 // The kernel is launched with programmatic stream serialization and touches global memory
 // only after griddepcontrol.wait.  No wait is unbounded: mbarrier waits give up after 2 s
 // (status bit, clean exit through the remaining barriers); every CTA executes every cluster
@@ -825,6 +825,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bar[s], 1);
+    mbar_init(&bar[S + 2], 1);       // the combine's partials
     fence_mbar_init();
     s_abort = 0;
   }
@@ -1775,8 +1776,9 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     }
   }
   // ---- combine: each CTA pushes the quads of its partial that rank r owns, with its (m, l),
-  // into rank r's list region (remote stores, no round trip); one cluster barrier; each CTA
-  // then merges its slice of the G*D outputs from local shared memory, in rank order.
+  // into rank r's list region by st.async stores whose bytes complete on rank r's combine
+  // mbarrier; each CTA waits for its own slice only (no cluster barrier), then merges its
+  // slice of the G*D outputs from local shared memory, in rank order.
   constexpr int kQuads = G * D / 4;
   const int qper = (kQuads + CL - 1) / CL;
   float4* comb_q = reinterpret_cast<float4*>(list);                 // [CL][qper] partial quads
@@ -1813,11 +1815,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       } else {
         v = reinterpret_cast<const float4*>(part)[qi];
       }
-      if constexpr (FAST)
-        st_async_v4(cluster_addr(smem_u32(comb_q + rank * qper + k), r), v,
-                    cluster_addr(smem_u32(&bar[S + 2]), r));
-      else
-        cluster.map_shared_rank(comb_q, r)[rank * qper + k] = v;
+      st_async_v4(cluster_addr(smem_u32(comb_q + rank * qper + k), r), v,
+                  cluster_addr(smem_u32(&bar[S + 2]), r));
     }
     if (tid < CL * G) {
       const int r = tid / G, g = tid - r * G;
@@ -1838,26 +1837,16 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         pm = part_m[g];
         pl = part_l[g];
       }
-      if constexpr (FAST) {
-        st_async_v2(cluster_addr(smem_u32(comb_ml + (rank * G + g) * 2), r), pm, pl,
-                    cluster_addr(smem_u32(&bar[S + 2]), r));
-      } else {
-        float* dst = cluster.map_shared_rank(comb_ml, r) + (rank * G + g) * 2;
-        dst[0] = pm;
-        dst[1] = pl;
-      }
+      st_async_v2(cluster_addr(smem_u32(comb_ml + (rank * G + g) * 2), r), pm, pl,
+                  cluster_addr(smem_u32(&bar[S + 2]), r));
     }
-    if constexpr (FAST) {
-      // this CTA's slice of every peer's partial (and their (m, l)) has arrived: the bytes
-      // counted on its mbarrier, no cluster-wide barrier
-      if (tid == 0) {
-        const int nq_own = min(min(rank * qper, kQuads) + qper, kQuads) - min(rank * qper, kQuads);
-        mbar_arrive_expect_tx(&bar[S + 2], static_cast<uint32_t>(CL * (nq_own * 16 + G * 8)));
-      }
-      if (!mbar_wait(&bar[S + 2], 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
-    } else {
-      cluster.sync();                                               // barrier D1: delivered
+    // this CTA's slice of every peer's partial (and their (m, l)) has arrived: the bytes
+    // counted on its mbarrier, no cluster-wide barrier
+    if (tid == 0) {
+      const int nq_own = min(min(rank * qper, kQuads) + qper, kQuads) - min(rank * qper, kQuads);
+      mbar_arrive_expect_tx(&bar[S + 2], static_cast<uint32_t>(CL * (nq_own * 16 + G * 8)));
     }
+    if (!mbar_wait(&bar[S + 2], 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
   }
   float* out_unit = p.out + (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D;
   if (attending && FAST) {
