@@ -1849,7 +1849,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     if (!mbar_wait(&bar[S + 2], 0)) set_status(p.status, SANTA_DEV_TIMEOUT);
   }
   float* out_unit = p.out + (static_cast<int64_t>(b) * p.num_q_heads + h * G) * D;
-  if (attending && FAST) {
+  if (attending && NC == 1) {
     // this CTA's slice of the output: each thread forms the CL ranks' weights of its quad's
     // head itself and merges in rank order (no barrier)
     const int q0 = min(rank * qper, kQuads);
@@ -1933,48 +1933,36 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   __syncthreads();
   if (!s_last) return;
   // every load of this CTA at once (one round trip): thread t's quad of every cluster partial
-  // (G * d / 4 <= 256 quads) and, for t < NC * G, one cluster's (m, l) of one head
+  // (G * d / 4 <= 256 quads) and the clusters' (m, l) of its head; each thread then forms
+  // its head's weights itself and merges in cluster order (no barrier)
   static_assert(G * D / 4 <= 256, "one output quad per thread");
   const int qi = tid, gq = (qi * 4) / D;
-  float4 v[kMaxClustersPerUnit];
-  {
+  if (qi < kQuads) {
+    float4 v[kMaxClustersPerUnit];
+    float2 ml[kMaxClustersPerUnit];
     const float4* src =
         reinterpret_cast<const float4*>(p.part_acc + static_cast<int64_t>(unit) * NC * G * D) + qi;
+    const float2* mls = reinterpret_cast<const float2*>(p.part_ml) +
+                        static_cast<int64_t>(unit) * NC * G + gq;
 #pragma unroll
-    for (int c = 0; c < kMaxClustersPerUnit; ++c)
-      v[c] = (c < NC && qi < kQuads) ? __ldcg(src + c * (G * D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  if (tid < NC * G) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) +
-                             static_cast<int64_t>(unit) * NC * G + tid);
-    s_pm[tid] = ml.x;
-    s_pz[tid] = ml.y;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float mx = kNegInf;
-    for (int c = 0; c < NC; ++c) mx = fmaxf(mx, s_pm[c * G + tid]);
-    float l = 0.f;
-    for (int c = 0; c < NC; ++c) {
-      const float mc = s_pm[c * G + tid];
-      const float w = mc == kNegInf ? 0.f : exp2f(mc - mx);
-      s_pm[c * G + tid] = w;
-      l = fmaf(w, s_pz[c * G + tid], l);
+    for (int c = 0; c < kMaxClustersPerUnit; ++c) {
+      v[c] = c < NC ? __ldcg(src + c * (G * D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      ml[c] = c < NC ? __ldcg(mls + c * G) : make_float2(kNegInf, 0.f);
     }
-    s_gz[tid] = l;
-  }
-  __syncthreads();
-  if (qi < kQuads) {
+    float mx = kNegInf;
+#pragma unroll
+    for (int c = 0; c < kMaxClustersPerUnit; ++c) mx = fmaxf(mx, ml[c].x);
+    float l = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < kMaxClustersPerUnit; ++c) {
-      const float w = c < NC ? s_pm[c * G + gq] : 0.f;
+      const float w = ml[c].x == kNegInf ? 0.f : ex2_approx(ml[c].x - mx);
+      l = fmaf(w, ml[c].y, l);
       a.x = fmaf(w, v[c].x, a.x);
       a.y = fmaf(w, v[c].y, a.y);
       a.z = fmaf(w, v[c].z, a.z);
       a.w = fmaf(w, v[c].w, a.w);
     }
-    const float l = s_gz[gq];
     const float inv = l > 0.f ? 1.f / l : 0.f;
     reinterpret_cast<float4*>(out_unit)[qi] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
   }
