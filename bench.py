@@ -871,6 +871,16 @@ def _mean_ci(xs):
     return m, 1.96 * sd / math.sqrt(n)
 
 
+def _drop_host_stalls(us, factor=20.0):
+    """Steps that took more than `factor` times the median: the host fell behind the spin
+    kernel that precedes each step, and the device waited for the next launch inside the
+    timed interval (a Python or OS pause of milliseconds against steps of microseconds).
+    Returns the remaining steps and how many were dropped."""
+    med = statistics.median(us)
+    kept = [u for u in us if u <= factor * med]
+    return kept, len(us) - len(kept)
+
+
 def run_loop(args):
     """A generation at the workload's context (the explainer's pitfall 2: sampling variance
     over autoregressive steps).  Every step appends the next token's K/V (santa_append_kv)
@@ -962,9 +972,10 @@ def run_loop(args):
         if R is None:
             dense_out.copy_(outs)
         us = [a.elapsed_time(b) * 1e3 for a, b in ev]
-        m, ci = _mean_ci(us)
+        kept, stalls = _drop_host_stalls(us)
+        m, ci = _mean_ci(kept)
         row = {"policy": name, "refresh": R, "step_us_mean": m, "step_us_ci95": ci,
-               "step_us_p50": statistics.median(us)}
+               "step_us_p50": statistics.median(us), "host_stall_steps_dropped": stalls}
         if R is not None:
             diff = (outs - dense_out).double()
             ref = dense_out.double()
@@ -986,7 +997,9 @@ def run_loop(args):
         "draws": cfg.draws, "results": results,
         "l2": "flushed before every step (a write of 2x the L2 size)",
         "timing": "CUDA events around each step's append + decode; a spin kernel before "
-                  "every step keeps the device behind the host, so no launch gap is timed",
+                  "every step keeps the device behind the host, so no launch gap is timed; "
+                  "steps above 20x the median (the host fell behind the spin) are left out "
+                  "of the mean and counted",
         "queries": "per step: each head's mixture part fixed, fresh 0.3 * N(0, I) noise",
         "error": "||out - dense|| / ||dense|| per query head, mean over heads; accumulated: "
                  "the same for the outputs summed over the first t steps"}))

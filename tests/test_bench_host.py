@@ -96,3 +96,12 @@ def test_traffic_record_from_an_ncu_log(bench, tmp_path):
     assert rec["dram_bytes_per_launch"] == (8.17e6 + 7915008.0 + 1500.0) / 2
     assert rec["kernel_source_sha"] == bench.kernel_source_sha()
     assert json.loads(out.read_text()) == rec
+
+
+def test_host_stall_filter(bench):
+    """Loop-mode steps far above the median (the host fell behind the spin kernel) are left
+    out of the mean and counted; ordinary spread is kept."""
+    us = [17.0, 17.2, 16.9, 17.1, 50000.0, 17.0, 30.0]
+    kept, dropped = bench._drop_host_stalls(us)
+    assert dropped == 1 and 50000.0 not in kept and 30.0 in kept
+    assert bench._drop_host_stalls([5.0] * 10) == ([5.0] * 10, 0)
