@@ -259,10 +259,10 @@ int santa_decode(const santa_decode_args* a, void* stream);
 /*
  * santa_decode_path — which form of the kernel santa_decode(a) runs (a's pointers need not
  * be valid; shapes, sampler, mix_alpha and workspace_bytes are read).  1: the compact form,
- * for bf16 steps with i.i.d. Horvitz-Thompson draws, no mixture, one cluster per unit and at
- * most 1024 teams per sequence, whose sampling prologue is compiled without the general
- * form's branches; 0: the general form; a negative santa_status for a refused shape.  Both
- * forms compute the same step.
+ * for bf16 steps with one cluster per unit and at most 1024 teams per sequence, whose
+ * sampling prologue is compiled without the general form's branches (the sampler variants
+ * and the mixture run separate instantiations of it); 0: the general form; a negative
+ * santa_status for a refused shape.  Both forms compute the same step.
  */
 int santa_decode_path(const santa_decode_args* a);
 

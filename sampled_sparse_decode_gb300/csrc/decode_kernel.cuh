@@ -42,8 +42,8 @@
 //            completing on rank r's mbarrier); each CTA merges its slice in rank order.
 //            With NC > 1 the cluster partials go to global scratch and the last CTA of the
 //            unit (an atomic ticket, no waiting) merges them in cluster order.
-// Compact form (template flag FAST: a bf16 decode step with i.i.d. Horvitz-Thompson draws,
-// no mixture, NC = 1).  Phases A and B are replaced by a shorter sequence: CTA r stages its
+// Compact form (template flag FAST: a bf16 decode step with NC = 1; FAST = 1 compiles the
+// i.i.d. Horvitz-Thompson draws alone, FAST = 2 adds the sampler variants and the mixture).  Phases A and B are replaced by a shorter sequence: CTA r stages its
 // slice's representative rows by one bulk copy each, scores them in base 2, and stores its
 // [G + 1][slice] block (scores, page ids) into every CTA with st.async, completing on the
 // receiver's mbarrier (no cluster barrier); each CTA then takes the per-head statistics
@@ -142,8 +142,7 @@ struct DecodeTraits {
   static constexpr int kMinBlocks = (!W && kSmem <= 112 * 1024) ? 2 : 1;
   static_assert(!W || (BF16 && kStages % 2 == 0), "wide: bf16 only, even stage count");
 
-  // Compact path (a decode step with i.i.d. Horvitz-Thompson draws, no mixture, one cluster
-  // per unit).  CTA r scores the slice of `fast_per` teams starting at r * fast_per (a power
+  // Compact path (a bf16 decode step with one cluster per unit).  CTA r scores the slice of `fast_per` teams starting at r * fast_per (a power
   // of two >= 4, so each slice is a whole number of 16-byte pieces and team j's rank and
   // place in it are shifts) and sends its block [G + 1][fast_per] (the G heads' scores, then
   // the page ids) from its list region to every CTA, into block r of the receive buffer
@@ -429,7 +428,7 @@ __device__ __forceinline__ void score_teams(const DecodeParams& p, int b, int h,
 
 // ---------------------------------------------------------------- the kernel
 
-template <bool BF16, int D, int G, bool W, bool FAST = false>
+template <bool BF16, int D, int G, bool W, int FAST = 0>
 __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks))
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using Tr = DecodeTraits<BF16, D, G, W>;
@@ -496,10 +495,12 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   };
   if constexpr (FAST) {
     // ============================================================ compact path: phases A, B
-    // A decode step with i.i.d. draws and Horvitz-Thompson weights, no mixture, one cluster
-    // per unit, every team of the unit sampled in each CTA (DecodeTraits::fast_fits).  This
-    // code runs once per launch, so it is kept short (rolled loops) and has few phases: the
-    // SM waits on fetching straight-line instructions here more than on the arithmetic.
+    // A decode step with one cluster per unit, every team of the unit sampled in each CTA
+    // (DecodeTraits::fast_fits).  FAST = 1: i.i.d. draws with Horvitz-Thompson weights and no
+    // mixture; FAST = 2 also compiles the sampler variants and the mixture (separate
+    // instantiations: the default sampler's prologue measured slower with their code in it).
+    // This code runs once per launch, so it is kept short (rolled loops) and has few phases:
+    // the SM waits on fetching straight-line instructions here more than on the arithmetic.
     const int n_max = p.max_teams;
     const int per = Tr::fast_per(n_max, CL);           // teams scored per CTA, power of 2
     const int lo = rank * per;
@@ -687,6 +688,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     // ---- p_j = sum_g e_gj / (G z_g), round(p_j 2^62) and the exact integer CDF (this
     // thread's inclusive sums, then one block-wide scan)
     unsigned long long run = 0ull;
+    const float alpha = FAST == 2 ? p.mix_alpha : 0.f;  // defensive mixture: q = (1 - a) p + a / n
+    const float alpha_n = n > 0 ? alpha / static_cast<float>(n) : 0.f;
 #pragma unroll 1
     for (int u = 0; u < tpt; ++u) {
       const int j = jt + u;
@@ -694,6 +697,8 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         float pj = 0.f;
 #pragma unroll
         for (int g = 0; g < G; ++g) pj = fmaf(xs[at(j, g)], zg[g], pj);
+        if constexpr (FAST == 2)
+          if (alpha != 0.f && j < n) pj = fmaf(1.f - alpha, pj, alpha_n);
         unsigned long long P = 0ull;
         if (pj > 0.f) {
           const float x = pj * 0x1p62f;                              // exact scaling
@@ -703,9 +708,17 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
         }
         run += P;
         cdf[j] = run;                 // this thread's inclusive sum; its prefix is added below
-        // pi_j = 1 - (1 - p_j)^M and the weight -log2 pi_j (to the team's head-0 entry of
-        // the receive buffer, no longer read); independent of the scan below
-        const float piv = -expm1f(static_cast<float>(M) * log1pf(-pj));
+        // 1 / weight and its -log2 (to the team's head-0 entry of the receive buffer, no
+        // longer read), independent of the scan below: Horvitz-Thompson pi_j = 1 - (1 - q_j)^M,
+        // systematic min(1, M q_j); Hansen-Hurwitz needs the draw counts, so q_j waits here
+        const float Mf = static_cast<float>(M);
+        float piv;
+        if constexpr (FAST == 2)
+          piv = p.sampler == SANTA_SAMPLER_SYSTEMATIC ? fminf(1.f, Mf * pj)
+                : p.sampler == SANTA_SAMPLER_IID_HH   ? pj
+                                                      : -expm1f(Mf * log1pf(-pj));
+        else
+          piv = -expm1f(Mf * log1pf(-pj));
         ps[j] = piv;
         xs[at(j, 0)] = -log2f(piv);
         flg[j] = 0;
@@ -722,15 +735,28 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     // ---- M draws: the smallest j with floor(u Z) < C_j
     const bool valid = len_ok && Z > 0ull;
     if (valid) {
+      // systematic: every point derives from the uniform of draw 0
+      const bool systematic = FAST == 2 && p.sampler == SANTA_SAMPLER_SYSTEMATIC;
 #pragma unroll 1
       for (int r = tid; r < M; r += Tr::kThreads) {
-        const uint32_t x = r == tid ? s_xw[r]
-                                    : philox4x32_10_compact(make_uint4(static_cast<uint32_t>(r),
-                                                                       static_cast<uint32_t>(h),
-                                                                       static_cast<uint32_t>(b), 0u),
-                                                            key).x;
+        uint32_t x;
+        if constexpr (FAST == 2) {
+          const int rw = systematic ? 0 : r;
+          x = rw < Tr::kThreads
+                  ? s_xw[rw]
+                  : philox4x32_10_compact(make_uint4(static_cast<uint32_t>(rw),
+                                                     static_cast<uint32_t>(h),
+                                                     static_cast<uint32_t>(b), 0u), key).x;
+        } else {
+          x = r == tid ? s_xw[r]
+                       : philox4x32_10_compact(make_uint4(static_cast<uint32_t>(r),
+                                                          static_cast<uint32_t>(h),
+                                                          static_cast<uint32_t>(b), 0u), key).x;
+        }
         const unsigned long long a = 2ull * x + 1ull;                // u = a / 2^33
-        const unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
+        unsigned long long t = (__umul64hi(a, Z) << 31) | ((a * Z) >> 33);
+        if constexpr (FAST == 2)
+          if (systematic) t = systematic_point(t, r, M, Z);
         int lo_i = 0, hi_i = n_max - 1;
 #pragma unroll 1
         while (lo_i < hi_i) {
@@ -738,7 +764,12 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
           if (t < cdf[mid]) hi_i = mid; else lo_i = mid + 1;
         }
         if (out_writer) p.draw_ids[static_cast<int64_t>(unit) * M + r] = lo_i;
-        flg[lo_i] = 1;
+        if constexpr (FAST == 2) {
+          if (p.sampler == SANTA_SAMPLER_IID_HH) atomicAdd(&flg[lo_i], 1);   // draws per team
+          else flg[lo_i] = 1;
+        } else {
+          flg[lo_i] = 1;
+        }
       }
     } else if (out_writer) {
 #pragma unroll 1
@@ -764,6 +795,13 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       for (int u = 0; u < tpt; ++u) {
         const int j = jt + u;
         if (j < n_max && flg[j]) {
+          if constexpr (FAST == 2) {
+            if (p.sampler == SANTA_SAMPLER_IID_HH) {   // 1 / weight = M q_j / c_j
+              const float recip = static_cast<float>(M) * ps[j] / static_cast<float>(flg[j]);
+              ps[j] = recip;
+              xs[at(j, 0)] = -log2f(recip);
+            }
+          }
           if (out_writer) {
             p.sel_ids[static_cast<int64_t>(unit) * M + k] = j;
             p.pi[static_cast<int64_t>(unit) * M + k] = ps[j];
@@ -1971,13 +2009,13 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
 
 // ---------------------------------------------------------------- host-side launch helpers
 
-template <bool BF16, int D, int G, bool W, bool FAST = false>
+template <bool BF16, int D, int G, bool W, int FAST = 0>
 std::atomic<unsigned long long>& decode_smem_flag() {
   static std::atomic<unsigned long long> flag{0};
   return flag;
 }
 
-template <bool BF16, int D, int G, bool W, bool FAST = false>
+template <bool BF16, int D, int G, bool W, int FAST = 0>
 cudaError_t decode_prepare_t() {
   using Tr = DecodeTraits<BF16, D, G, W>;
   auto* kern = decode_kernel<BF16, D, G, W, FAST>;
@@ -1996,7 +2034,7 @@ cudaError_t decode_prepare_t() {
 }
 
 // How many clusters of `cluster` CTAs can be co-resident (0 if none / on error).
-template <bool BF16, int D, int G, bool W, bool FAST = false>
+template <bool BF16, int D, int G, bool W, int FAST = 0>
 int decode_max_clusters_t(int cluster) {
   using Tr = DecodeTraits<BF16, D, G, W>;
   if (decode_prepare_t<BF16, D, G, W, FAST>() != cudaSuccess) return 0;
@@ -2017,7 +2055,7 @@ int decode_max_clusters_t(int cluster) {
   return n;
 }
 
-template <bool BF16, int D, int G, bool W, bool FAST = false>
+template <bool BF16, int D, int G, bool W, int FAST = 0>
 int decode_resident_t() {
   using Tr = DecodeTraits<BF16, D, G, W>;
   if (decode_prepare_t<BF16, D, G, W, FAST>() != cudaSuccess) return 0;
@@ -2028,7 +2066,7 @@ int decode_resident_t() {
   return blocks;
 }
 
-template <bool BF16, int D, int G, bool W, bool FAST = false>
+template <bool BF16, int D, int G, bool W, int FAST = 0>
 cudaError_t decode_launch_t(const DecodeParams& p, dim3 grid, int cluster, cudaStream_t stream) {
   using Tr = DecodeTraits<BF16, D, G, W>;
   cudaError_t e = decode_prepare_t<BF16, D, G, W, FAST>();

@@ -127,9 +127,10 @@ cudaError_t decode_launch_bf16_wide(const DecodeParams& p, int head_dim, int gro
                                     int cluster, cudaStream_t stream);
 int decode_resident_bf16_wide(int head_dim, int group);
 int decode_max_clusters_bf16_wide(int head_dim, int group, int cluster);
-// compact path (bf16 decode steps with i.i.d. Horvitz-Thompson draws, no mixture, one
-// cluster per unit, every team sampled in each CTA): launchers of both variants, the shape
-// test and the resident CTAs per SM (the plan is made for the general kernel's)
+// compact path (bf16 decode steps with one cluster per unit, every team sampled in each CTA;
+// these instantiations: i.i.d. Horvitz-Thompson draws, no mixture): launchers of both
+// variants, the shape test and the resident CTAs per SM (the plan is made for the general
+// kernel's)
 cudaError_t decode_launch_bf16_fast(const DecodeParams& p, int head_dim, int group, dim3 grid,
                                     int cluster, cudaStream_t stream);
 cudaError_t decode_launch_bf16_wide_fast(const DecodeParams& p, int head_dim, int group,
@@ -140,6 +141,14 @@ bool decode_fast_fits_bf16_wide(int head_dim, int group, int max_teams, int clus
                                 int team_size, int num_draws);
 int decode_resident_bf16_fast(int head_dim, int group);
 int decode_resident_bf16_wide_fast(int head_dim, int group);
+// the compact path with the sampler variants compiled in (systematic, Hansen-Hurwitz, the
+// defensive mixture): separate instantiations, so the default sampler's prologue stays short
+cudaError_t decode_launch_bf16_fast_var(const DecodeParams& p, int head_dim, int group,
+                                        dim3 grid, int cluster, cudaStream_t stream);
+cudaError_t decode_launch_bf16_wide_fast_var(const DecodeParams& p, int head_dim, int group,
+                                             dim3 grid, int cluster, cudaStream_t stream);
+int decode_resident_bf16_fast_var(int head_dim, int group);
+int decode_resident_bf16_wide_fast_var(int head_dim, int group);
 
 // Every host-side check santa_decode makes on `a`, then its launch plan; launches nothing
 // and touches no device memory.  On SANTA_OK *clusters_per_unit receives the plan's NC (> 1:

@@ -127,15 +127,18 @@ int resident_ctas(bool bf16, int d, int G, bool wide) {
 }
 
 // CTAs of the compact form of the bf16 kernel one SM holds (cached per device and shape).
-int compact_resident(int d, int G, bool wide) {
+int compact_resident(int d, int G, bool wide, bool variants) {
   static std::mutex mu;
-  static int cache[64][2][2][santa::kMaxGroup + 1] = {};
+  static int cache[64][2][2][2][santa::kMaxGroup + 1] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  int& c = cache[dev][wide][d == 128][G];
+  int& c = cache[dev][variants][wide][d == 128][G];
   if (!c)
-    c = wide ? santa::decode_resident_bf16_wide_fast(d, G) : santa::decode_resident_bf16_fast(d, G);
+    c = variants ? (wide ? santa::decode_resident_bf16_wide_fast_var(d, G)
+                         : santa::decode_resident_bf16_fast_var(d, G))
+                 : (wide ? santa::decode_resident_bf16_wide_fast(d, G)
+                         : santa::decode_resident_bf16_fast(d, G));
   return c;
 }
 
@@ -352,11 +355,11 @@ int encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int d) {
 }
 
 // Whether a checked and planned call runs the compact path of the decode kernel: a bf16
-// decode step with i.i.d. Horvitz-Thompson draws, no mixture and one cluster per unit, whose
-// shape the compact path's shared-memory layout holds.
+// decode step with one cluster per unit whose shape the compact path's shared-memory layout
+// holds.  The sampler variants and the mixture run its separate instantiations.
 bool uses_compact_path(const santa_decode_args* a, int mode, const Plan& pl) {
   if (mode != santa::kModeDecode || a->dtype != SANTA_BF16 || pl.clusters != 1) return false;
-  if (a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f) return false;
+  const bool variants = a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f;
   const int G = a->num_q_heads / a->num_kv_heads;
   const bool fits =
       pl.wide ? santa::decode_fast_fits_bf16_wide(a->head_dim, G, a->max_teams, pl.cluster,
@@ -364,8 +367,8 @@ bool uses_compact_path(const santa_decode_args* a, int mode, const Plan& pl) {
               : santa::decode_fast_fits_bf16(a->head_dim, G, a->max_teams, pl.cluster,
                                              a->team_size, a->num_draws);
   // the plan assumes the general kernel's resident CTAs per SM: the compact one must match
-  return fits &&
-         compact_resident(a->head_dim, G, pl.wide) >= resident_ctas(true, a->head_dim, G, pl.wide);
+  return fits && compact_resident(a->head_dim, G, pl.wide, variants) >=
+                     resident_ctas(true, a->head_dim, G, pl.wide);
 }
 
 // Every host-side check of a call in `mode`, then its plan; launches nothing.
@@ -440,6 +443,11 @@ int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   const dim3 grid(pl.cluster * pl.clusters, a->num_kv_heads, a->batch);
   const int G = a->num_q_heads / a->num_kv_heads;
   if (uses_compact_path(a, mode, pl)) {
+    if (a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f)
+      return map_cuda(pl.wide ? santa::decode_launch_bf16_wide_fast_var(p, a->head_dim, G, grid,
+                                                                        pl.cluster, stream)
+                              : santa::decode_launch_bf16_fast_var(p, a->head_dim, G, grid,
+                                                                   pl.cluster, stream));
     return map_cuda(pl.wide ? santa::decode_launch_bf16_wide_fast(p, a->head_dim, G, grid,
                                                                   pl.cluster, stream)
                             : santa::decode_launch_bf16_fast(p, a->head_dim, G, grid,

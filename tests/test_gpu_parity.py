@@ -69,17 +69,19 @@ def test_both_kernel_variants_are_covered():
 
 
 def test_compact_and_general_forms_are_both_covered():
-    """bf16 decode steps with the default sampler run the compact form of the kernel (both
-    variants); fp32 steps, sampler variants, a mixture and units spread over several clusters
-    run the general form.  The parity tests below cover each."""
+    """bf16 decode steps run the compact form of the kernel (both variants, every sampler and
+    the mixture); fp32 steps and units spread over several clusters run the general form, and
+    so do the sampling-only, attention-only and dense modes.  The parity tests below cover
+    each."""
     cases = [("qwen_b2_ragged", {}, "compact"), ("bf16_d64_t64", {}, "compact"),
              ("qwen_b40_two_per_sm", {}, "compact"), ("llama_paged_b4", {}, "compact"),
              ("long_paged_b2", {}, "compact"), ("qwen_b3_mixed_m64", {}, "compact"),
              ("long_b1_multicluster", {}, "compact"),
              ("tiny_f32", {}, "general"), ("f32_d128_g8", {}, "general"),
              ("f32_b1_two_clusters", {}, "general"),
-             ("qwen_b2_ragged", dict(sampler="systematic"), "general"),
-             ("qwen_b2_ragged", dict(mix_alpha=0.05), "general")]
+             ("qwen_b2_ragged", dict(sampler="systematic"), "compact"),
+             ("qwen_b2_ragged", dict(sampler="iid_hh"), "compact"),
+             ("qwen_b2_ragged", dict(mix_alpha=0.05), "compact")]
     for name, kw, want in cases:
         wl = make(SMALL[name])
         dw = DeviceWorkload(wl)
