@@ -42,16 +42,17 @@
 //            completing on rank r's mbarrier); each CTA merges its slice in rank order.
 //            With NC > 1 the cluster partials go to global scratch and the last CTA of the
 //            unit (an atomic ticket, no waiting) merges them in cluster order.
-// Compact form (template flag FAST: a bf16 decode step with NC = 1; FAST = 1 compiles the
-// i.i.d. Horvitz-Thompson draws alone, FAST = 2 adds the sampler variants and the mixture).  Phases A and B are replaced by a shorter sequence: CTA r stages its
-// slice's representative rows by one bulk copy each, scores them in base 2, and stores its
-// [G + 1][slice] block (scores, page ids) into every CTA with st.async, completing on the
-// receiver's mbarrier (no cluster barrier); each CTA then takes the per-head statistics
-// (warp per head), p and the CDF (one block scan), the draws (binary search, Philox words
-// computed while the rows were in flight), pi for every team, and writes S with the chunk
-// table in one pass, issuing the first copies at once.  In phase D each merging thread forms
-// its head's weights itself.  Its code is kept short: it runs once per launch, and the SM
-// waits on fetching cold instructions there.
+// Compact form (template flag FAST, bf16 steps with NC = 1).  FAST = 1 compiles a decode
+// step with i.i.d. Horvitz-Thompson draws alone; FAST = 2 adds the sampler variants, the
+// mixture and sampling-only steps.  Phases A and B are replaced by a shorter sequence: CTA r
+// stages its slice's representative rows by one bulk copy each, scores them in base 2, and
+// stores its [G + 1][slice] block (scores, page ids) into every CTA with st.async, completing
+// on the receiver's mbarrier (no cluster barrier); each CTA then takes the per-head
+// statistics (warp per head), p, pi and the CDF (one block scan), the draws (binary search,
+// Philox words computed while the rows were in flight), and writes S with the chunk table in
+// one pass, issuing the first copies at once.  In phase D each merging thread forms its
+// head's weights itself.  Its code is kept short: it runs once per launch, and the SM waits
+// on fetching cold instructions there.
 // The kernel is launched with programmatic stream serialization and touches global memory
 // only after griddepcontrol.wait.  No wait is unbounded: mbarrier waits give up after 2 s
 // (status bit, clean exit through the remaining barriers); every CTA executes every cluster
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
   const int unit = b * p.num_kv_heads + h;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, lane16 = lane & 15;
   const int M = p.num_draws;
-  const int mode = FAST ? kModeDecode : p.mode;
+  const int mode = FAST == 1 ? kModeDecode : p.mode;   // FAST = 2: decode or sample only
   const bool sampling = mode == kModeDecode || mode == kModeSample;
   const bool attending = mode != kModeSample;
   const bool writer = cidx == 0;          // the cluster that writes the sampling outputs
@@ -528,8 +529,10 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
     if (!bad_layout) {
       // shared memory only: allowed before the previous kernel of the stream has finished
       if (tid == 0) {
-        prefetch_tensormap(&p.tmap_k);
-        prefetch_tensormap(&p.tmap_v);
+        if (attending) {
+          prefetch_tensormap(&p.tmap_k);
+          prefetch_tensormap(&p.tmap_v);
+        }
         for (int s2 = 0; s2 < S; ++s2) mbar_init(&bar[s2], 1);
         mbar_init(rbar, Tr::kThreads);
         mbar_init(xbar, 1);
@@ -787,7 +790,7 @@ __global__ void __launch_bounds__(256, (DecodeTraits<BF16, D, G, W>::kMinBlocks)
       int tot;
       int k = block_exclusive_scan<int>(cnt, s_wi, tot);
       const int cpt = p.team_size / kChunk;
-      const int total_chunks = tot * cpt;
+      const int total_chunks = attending ? tot * cpt : 0;
       const int cps = (total_chunks + CL - 1) / CL;
       const int c_begin = min(rank * cps, total_chunks);
       n_chunks = min(total_chunks - c_begin, cps);

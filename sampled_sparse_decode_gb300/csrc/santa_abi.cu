@@ -354,12 +354,20 @@ int encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int d) {
   return r == CUDA_SUCCESS ? SANTA_OK : SANTA_ERR_CUDA;
 }
 
+// Whether a compact-path call needs the instantiations with the sampler variants compiled in:
+// a variant sampler, the mixture, or a sampling-only step.
+bool compact_variants(const santa_decode_args* a, int mode) {
+  return mode == santa::kModeSample || a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f;
+}
+
 // Whether a checked and planned call runs the compact path of the decode kernel: a bf16
-// decode step with one cluster per unit whose shape the compact path's shared-memory layout
-// holds.  The sampler variants and the mixture run its separate instantiations.
+// decode (or sampling-only) step with one cluster per unit whose shape the compact path's
+// shared-memory layout holds.
 bool uses_compact_path(const santa_decode_args* a, int mode, const Plan& pl) {
-  if (mode != santa::kModeDecode || a->dtype != SANTA_BF16 || pl.clusters != 1) return false;
-  const bool variants = a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f;
+  if ((mode != santa::kModeDecode && mode != santa::kModeSample) || a->dtype != SANTA_BF16 ||
+      pl.clusters != 1)
+    return false;
+  const bool variants = compact_variants(a, mode);
   const int G = a->num_q_heads / a->num_kv_heads;
   const bool fits =
       pl.wide ? santa::decode_fast_fits_bf16_wide(a->head_dim, G, a->max_teams, pl.cluster,
@@ -443,7 +451,7 @@ int launch(const santa_decode_args* a, int mode, cudaStream_t stream) {
   const dim3 grid(pl.cluster * pl.clusters, a->num_kv_heads, a->batch);
   const int G = a->num_q_heads / a->num_kv_heads;
   if (uses_compact_path(a, mode, pl)) {
-    if (a->sampler != SANTA_SAMPLER_IID_HT || a->mix_alpha != 0.f)
+    if (compact_variants(a, mode))
       return map_cuda(pl.wide ? santa::decode_launch_bf16_wide_fast_var(p, a->head_dim, G, grid,
                                                                         pl.cluster, stream)
                               : santa::decode_launch_bf16_fast_var(p, a->head_dim, G, grid,

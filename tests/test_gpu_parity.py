@@ -70,9 +70,9 @@ def test_both_kernel_variants_are_covered():
 
 def test_compact_and_general_forms_are_both_covered():
     """bf16 decode steps run the compact form of the kernel (both variants, every sampler and
-    the mixture); fp32 steps and units spread over several clusters run the general form, and
-    so do the sampling-only, attention-only and dense modes.  The parity tests below cover
-    each."""
+    the mixture; bf16 sampling-only steps too); fp32 steps and units spread over several
+    clusters run the general form, and so do the attention-only and dense modes.  The parity
+    tests below cover each."""
     cases = [("qwen_b2_ragged", {}, "compact"), ("bf16_d64_t64", {}, "compact"),
              ("qwen_b40_two_per_sm", {}, "compact"), ("llama_paged_b4", {}, "compact"),
              ("long_paged_b2", {}, "compact"), ("qwen_b3_mixed_m64", {}, "compact"),
