@@ -316,6 +316,13 @@ int santa_decode_noalloc(const santa_decode_args* a, void* stream);
  * copies in_bytes from host_in to dev_in, runs santa_decode(a), copies out_bytes from
  * dev_out to host_out and waits for the stream.
  *
+ *   - How each copy is made: when the host buffer is page-locked memory that the current
+ *     device reaches at the same address (cudaHostAlloc, a pinned torch tensor) and both
+ *     pointers and the size are multiples of 16 bytes, a small kernel of this library moves
+ *     the bytes (reading or writing the host memory directly), chained to the decode launch
+ *     by programmatic dependent launch; otherwise cudaMemcpyAsync does.  The bytes moved are
+ *     the same either way.
+ *
  *   - The caller lays out the buffers.  a's input pointers (q, page_table, seq_lens) point
  *     into dev_in, and its output pointers (out, draw_ids, sel_ids, sel_count, pi, and
  *     device_status if the caller wants it back in the same copy) into dev_out, so that

@@ -356,10 +356,12 @@ class PreparedDecode:
         self._a = _args(q, k_pool, v_pool, reps, page_table, seq_lens, num_draws, 0,
                         self.bufs, sampler, mix_alpha)
         self._fn = lib().santa_decode
+        self._aref = ctypes.byref(self._a)
+        self._host_call = None      # (inputs, host, santa_decode_host's buffer arguments)
 
     def run(self, seed: int, stream=None) -> DecodeBuffers:
         self._a.seed = seed & 0xFFFFFFFFFFFFFFFF
-        _check(self._fn(ctypes.byref(self._a), _stream(stream)), "santa_decode")
+        _check(self._fn(self._aref, _stream(stream)), "santa_decode")
         return self.bufs
 
     def run_host(self, seed: int, inputs: StepInputs, host: HostOutputs,
@@ -368,18 +370,22 @@ class PreparedDecode:
         bufs.outputs -> host.slab, then a wait for the stream.  The PreparedDecode must have
         been made on inputs' device views and packed DecodeBuffers; host.device_status holds
         the step's status word (sticky: zero it in the device slab to clear it)."""
-        b = self.bufs
-        if (b.outputs is None or host.slab.numel() != b.outputs.numel() or
-                self._a.q != inputs.q.data_ptr() or
-                self._a.page_table != inputs.page_table.data_ptr() or
-                self._a.seq_lens != inputs.seq_lens.data_ptr()):
-            raise SantaError("run_host needs packed DecodeBuffers, their host_mirror() and a "
-                             "PreparedDecode made on the StepInputs' device views")
+        c = self._host_call
+        if c is None or c[0] is not inputs or c[1] is not host:
+            b = self.bufs
+            if (b.outputs is None or host.slab.numel() != b.outputs.numel() or
+                    self._a.q != inputs.q.data_ptr() or
+                    self._a.page_table != inputs.page_table.data_ptr() or
+                    self._a.seq_lens != inputs.seq_lens.data_ptr()):
+                raise SantaError("run_host needs packed DecodeBuffers, their host_mirror() "
+                                 "and a PreparedDecode made on the StepInputs' device views")
+            # checked once per (inputs, host) pair: their storage may not change afterwards
+            c = self._host_call = (inputs, host, lib().santa_decode_host,
+                                   (inputs.host_slab.data_ptr(), inputs.slab.data_ptr(),
+                                    inputs.slab.numel(), host.slab.data_ptr(),
+                                    b.outputs.data_ptr(), b.outputs.numel()))
         self._a.seed = seed & 0xFFFFFFFFFFFFFFFF
-        _check(lib().santa_decode_host(ctypes.byref(self._a), inputs.host_slab.data_ptr(),
-                                       inputs.slab.data_ptr(), inputs.slab.numel(),
-                                       host.slab.data_ptr(), b.outputs.data_ptr(),
-                                       b.outputs.numel(), _stream(stream)), "santa_decode_host")
+        _check(c[2](self._aref, *c[3], _stream(stream)), "santa_decode_host")
         return host
 
 

@@ -75,6 +75,13 @@ struct AppendParams {
 };
 cudaError_t launch_append(const AppendParams& p, int head_dim, cudaStream_t stream);
 
+// ---------------------------------------------------------------- host slabs of santa_decode_host
+// bytes / 16 words from src to dst (both 16-byte aligned; one of them host memory mapped into
+// the device's address space).  stage-in lets the next launch be scheduled early; stage-out
+// is a programmatic dependent of the previous launch and reads nothing before it completed.
+cudaError_t launch_stage_in(const void* src, void* dst, size_t bytes, cudaStream_t stream);
+cudaError_t launch_stage_out(const void* src, void* dst, size_t bytes, cudaStream_t stream);
+
 // ---------------------------------------------------------------- fused decode step
 constexpr int kModeDecode = 0;   // sample, then attend over the sampled teams
 constexpr int kModeSample = 1;   // sample only

@@ -13,6 +13,26 @@
 
 namespace {
 
+// `host` itself, if it is page-locked memory that the current device reaches at the same
+// address (unified addressing) and the copy with `dev` can move 16-byte words (both pointers
+// and the size multiples of 16); otherwise nullptr, and santa_decode_host uses the copy
+// engine.  Pageable memory, memory pinned for another device and unaligned copies all take
+// the copy engine.
+const void* mapped_host(const void* host, const void* dev, size_t bytes) {
+  if (((reinterpret_cast<uintptr_t>(host) | reinterpret_cast<uintptr_t>(dev) | bytes) & 15) != 0)
+    return nullptr;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  int cur = -1;
+  if (at.type != cudaMemoryTypeHost || at.devicePointer != host ||
+      cudaGetDevice(&cur) != cudaSuccess || at.device != cur)
+    return nullptr;
+  return host;  // unified addressing: the device reaches the memory at the host's address
+}
+
 using santa::DecodeParams;
 using santa::RepsParams;
 
@@ -716,14 +736,22 @@ int santa_decode_host(const santa_decode_args* a, const void* host_in, void* dev
   if (!a || (in_bytes && (!host_in || !dev_in)) || (out_bytes && (!host_out || !dev_out)))
     return SANTA_ERR_INVALID_ARG;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (in_bytes &&
-      cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return SANTA_ERR_CUDA;
+  if (in_bytes) {
+    const void* src = mapped_host(host_in, dev_in, in_bytes);
+    const cudaError_t e =
+        src ? santa::launch_stage_in(src, dev_in, in_bytes, s)
+            : cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return SANTA_ERR_CUDA;
+  }
   const int rc = launch(a, santa::kModeDecode, s);
   if (rc != SANTA_OK) return rc;
-  if (out_bytes &&
-      cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return SANTA_ERR_CUDA;
+  if (out_bytes) {
+    void* dst = const_cast<void*>(mapped_host(host_out, dev_out, out_bytes));
+    const cudaError_t e =
+        dst ? santa::launch_stage_out(dev_out, dst, out_bytes, s)
+            : cudaMemcpyAsync(host_out, dev_out, out_bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return SANTA_ERR_CUDA;
+  }
   return cudaStreamSynchronize(s) == cudaSuccess ? SANTA_OK : SANTA_ERR_CUDA;
 }
 

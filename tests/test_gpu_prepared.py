@@ -98,3 +98,70 @@ def test_host_step_matches_santa_decode():
     with pytest.raises(santa.SantaError):
         santa.santa_decode_prepared(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table,
                                     dw.seq_lens, cfg.draws, bufs=pbufs).run_host(1, inp, host)
+
+
+def test_host_step_copy_routes_agree():
+    """santa_decode_host moves the slabs with its own copy kernels when the host buffers are
+    page-locked, mapped and 16-byte aligned, and with the copy engine otherwise (pageable
+    memory, unaligned pointers).  Every route gives the same host bytes, and new host
+    contents written between calls are the ones the step reads."""
+    import ctypes
+    from sampled_sparse_decode_gb300 import binding as Bn
+    wl = W.generate("qwen7b_32k_b8_m64", batch=2, seq_len=4000)
+    dw = DeviceWorkload(wl)
+    cfg = wl.cfg
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    inp = santa.StepInputs.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.head_dim,
+                                    wl.max_teams)
+    inp.host_page_table.copy_(dw.page_table.cpu())
+    inp.host_seq_lens.copy_(dw.seq_lens.cpu())
+    pbufs = santa.DecodeBuffers.allocate(dw.q.dtype, cfg.batch, cfg.q_heads, cfg.kv_heads,
+                                         cfg.head_dim, cfg.team_size, wl.max_teams, cfg.draws,
+                                         packed=True)
+    prep = santa.santa_decode_prepared(inp.q, dw.k_pool, dw.v_pool, reps, inp.page_table,
+                                       inp.seq_lens, cfg.draws, bufs=pbufs)
+    n_in, n_out = inp.slab.numel(), pbufs.outputs.numel()
+    stream = torch.cuda.current_stream()
+
+    def step(seed, host_in, host_out):
+        prep._a.seed = seed
+        rc = Bn.lib().santa_decode_host(ctypes.byref(prep._a), host_in.data_ptr(),
+                                        inp.slab.data_ptr(), n_in, host_out.data_ptr(),
+                                        pbufs.outputs.data_ptr(), n_out, stream.cuda_stream)
+        assert rc == 0
+        return host_out.clone()
+
+    pinned_in = torch.empty(n_in + 16, dtype=torch.uint8, pin_memory=True)
+    pinned_out = torch.empty(n_out + 16, dtype=torch.uint8, pin_memory=True)
+    pageable_in = torch.empty(n_in, dtype=torch.uint8)
+    pageable_out = torch.empty(n_out, dtype=torch.uint8)
+    assert pinned_in.data_ptr() % 16 == 0 and pinned_out.data_ptr() % 16 == 0
+    rng = np.random.default_rng(11)
+    for trial in range(3):
+        # new query contents for every trial, through the same host storage
+        q = W.f32_to_bf16_bits(rng.standard_normal(wl.q.shape).astype(np.float32))
+        inp.host_q.copy_(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16))
+        src = inp.host_slab
+        routes = {
+            "mapped": (pinned_in[:n_in], pinned_out[:n_out]),
+            "pageable": (pageable_in, pageable_out),
+            "unaligned": (pinned_in[8:8 + n_in], pinned_out[8:8 + n_out]),
+        }
+        got = {}
+        for name, (hin, hout) in routes.items():
+            hin.copy_(src)
+            hout.fill_(0xA5)
+            got[name] = step(40 + trial, hin, hout)
+        ref = santa.santa_decode(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16)
+                                 .to(dw.q.device), dw.k_pool, dw.v_pool, reps, dw.page_table,
+                                 dw.seq_lens, cfg.draws, 40 + trial)
+        torch.cuda.synchronize()
+        assert ref.status() == 0
+        for name in ("pageable", "unaligned"):
+            assert torch.equal(got[name], got["mapped"]), name
+        host = pbufs.host_mirror()
+        host.slab.copy_(got["mapped"])
+        assert int(host.device_status[0]) == 0
+        assert torch.equal(host.out, ref.out.cpu())
+        assert torch.equal(host.draw_ids, ref.draw_ids.cpu())
+        assert torch.equal(host.sel_count, ref.sel_count.cpu())
