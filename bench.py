@@ -23,8 +23,10 @@ dense      the in-run dense split-K decode kernel on the same buffers (speed ref
 workloads  the other full-size workloads (Qwen B=8 M=64, Llama paged B=16, 128K B=4) timed
            the same way, each with its roofline fraction and dense kernel, and the 128K
            workload's sweep over M in {16, 31, 64, 128}.
-timing     every entry point's K steps are replayed from CUDA graphs (each graph replayed
-           once before timing) behind a spin kernel, so the events time the device only.
+timing     every entry point's K steps run in one CUDA graph after one untimed step of the
+           same entry point; the start event waits only for that step, so the K steps are
+           timed as K step periods (each graph replayed untimed first, then once behind a
+           spin kernel, so the events time the device only).
 cpu_baseline  the fp64 C oracle, single-threaded, on a bounded sample of steps.
 --impl reference  times that oracle alone (the reference arm of this benchmark).
 """
@@ -364,8 +366,9 @@ def config_of(cfg, world):
             "parallelism": "replicas" if world > 1 else "1gpu",
             "l2": "inputs larger than L2: K, V and the representatives rotate over copies, "
                   ">= 6x the L2 size touched between two uses of a copy",
-            "timing": "CUDA graphs of whole steps, every graph replayed once before timing, "
-                      "CUDA events on the launching stream behind a spin kernel"}
+            "timing": "one CUDA graph per entry point: one untimed step, then the K timed "
+                      "steps; CUDA events (start after the untimed step, end after step K), "
+                      "the graph replayed untimed first, then timed behind a spin kernel"}
 
 
 def _dev_tensor(a, dev):
@@ -464,11 +467,14 @@ class Rig:
 
 
 class Timer:
-    """Exactly K steps of one entry point, replayed from CUDA graphs over a rig's rotation
-    copies: K // R replays of an R-step graph and one (K mod R)-step tail.  Every graph is
-    replayed once untimed (the tail first, so the last warm-up replay is the full graph and
-    every copy's reuse is R - 1 steps apart), at least W steps in all.  The timed replays are
-    enqueued behind a spin kernel, so the events time the device, not the host's launches."""
+    """Exactly K steps of one entry point, timed inside one CUDA graph over a rig's rotation
+    copies (step k uses copy k mod R, so a copy is reused R steps later).  The graph holds one
+    untimed step (copy R - 1), then the K timed steps.  The start event is recorded on a
+    branch that waits only for that untimed step, and the end event after step K, so the
+    interval is K step periods: the first timed step overlaps the tail of its predecessor,
+    as every later one does (programmatic dependent launch), and no graph boundary or launch
+    of the first kernel falls inside it.  The graph is replayed untimed until at least W steps
+    have run, then once more, enqueued behind a spin kernel, for the timing."""
 
     def __init__(self, dev, stream, world):
         self.dev, self.stream, self.world = dev, stream, world
@@ -478,46 +484,46 @@ class Timer:
         if rc:
             raise RuntimeError(f"{fn.__name__}: status {rc}")
 
-    def capture(self, body):
-        import torch
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(self.stream):
-            body()                                   # attribute set-up, lazy loading
-            self.stream.synchronize()
-            with torch.cuda.graph(g, stream=self.stream):
-                body()
-        return g
-
     def barrier(self):
         import torch
         if self.world > 1:
             torch.distributed.barrier()
 
-    def run(self, make, R, K, W_, label):
-        """make(n) -> a graph of n steps over rotations 0..n-1.  Returns (device seconds for
-        the K steps, (wall start, wall end))."""
+    def run(self, step, R, K, W_, label):
+        """step(r) enqueues one step on rotation copy r.  Returns (device seconds for the K
+        steps, (wall start, wall end))."""
         import torch
-        full, tail = divmod(K, R)
-        g_full = make(R)
-        g_tail = make(tail) if tail else None
+        e0, e1 = timing_event_pair()
+        fork = torch.cuda.Event()
+        side = torch.cuda.Stream(device=self.dev)
+
+        def body(capturing):
+            step(R - 1)                              # untimed: its tail overlaps step 0
+            if capturing:
+                fork.record(self.stream)
+                side.wait_event(fork)
+                e0.record(side)
+            for k in range(K):
+                step(k % R)
+            if capturing:
+                e1.record(self.stream)
+                self.stream.wait_stream(side)
+
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(self.stream):
-            if g_tail is not None:
-                g_tail.replay()
-            for _ in range(max(1, math.ceil(W_ / R))):
-                g_full.replay()
+            body(False)                              # attribute set-up, lazy loading
+            self.stream.synchronize()
+            with torch.cuda.graph(g, stream=self.stream):
+                body(True)
+            for _ in range(max(1, math.ceil(W_ / (K + 1)))):
+                g.replay()
         torch.cuda.synchronize(self.dev)
         self.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.nvtx.range_push(label)
         t0 = time.time()
         with torch.cuda.stream(self.stream):
             torch.cuda._sleep(SPIN_CYCLES)
-            e0.record(self.stream)
-            for _ in range(full):
-                g_full.replay()
-            if g_tail is not None:
-                g_tail.replay()
-            e1.record(self.stream)
+            g.replay()
         torch.cuda.synchronize(self.dev)
         t1 = time.time()
         torch.cuda.nvtx.range_pop()
@@ -526,9 +532,49 @@ class Timer:
 
     def steps(self, fn, a_list, K, W_, label):
         """Seconds per step of `fn` (an entry point taking a santa_decode_args) over a_list."""
-        make = lambda n: self.capture(lambda: [self.call(fn, a_list[r]) for r in range(n)])
-        sec, window = self.run(make, len(a_list), K, W_, label)
+        sec, window = self.run(lambda r: self.call(fn, a_list[r]), len(a_list), K, W_, label)
         return sec / K, window
+
+
+def timing_event_pair():
+    """Two timing events that become event-record nodes when recorded inside a graph capture
+    (torch.cuda.Event's `external` flag; older torch versions record them through the CUDA
+    runtime's cudaEventRecordWithFlags with cudaEventRecordExternal)."""
+    import torch
+    try:
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+    except TypeError:
+        return _ExternalEvent(), _ExternalEvent()
+
+
+class _ExternalEvent:
+    """A timing event recorded as an event-record node under graph capture."""
+    _rt = None
+
+    def __init__(self):
+        import torch
+        self.ev = torch.cuda.Event(enable_timing=True)
+        self.ev.record()                             # creates the CUDA event
+        torch.cuda.synchronize()
+
+    def record(self, stream):
+        if _ExternalEvent._rt is None:
+            import glob
+            import torch
+            names = sorted(glob.glob(os.path.join(os.path.dirname(torch.__file__), "lib",
+                                                  "libcudart.so*")) +
+                           glob.glob("/usr/local/cuda/lib64/libcudart.so*"))
+            rt = ctypes.CDLL(names[0])
+            rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                                    ctypes.c_uint]
+            _ExternalEvent._rt = rt
+        rc = _ExternalEvent._rt.cudaEventRecordWithFlags(self.ev.cuda_event, stream.cuda_stream, 1)
+        if rc:
+            raise RuntimeError(f"cudaEventRecordWithFlags: {rc}")
+
+    def elapsed_time(self, other):
+        return self.ev.elapsed_time(other.ev)
 
 
 def measure_workload(rig, timer, lib, K, W_, peak, draws=None, dense_s=None, sampler="iid_ht",
@@ -612,24 +658,21 @@ def run_ours(args):
     last = (rig.lens - 1).contiguous()
     nxt = torch.empty_like(rig.lens)
 
-    def append_make(n):
-        return timer.capture(lambda: [santa.santa_append_kv(kn, vn, rig.ks[r], rig.vs[r],
-                                                            rig.reps[r], rig.pt, last, nxt,
-                                                            stream=stream) for r in range(n)])
+    def append_step(r):
+        santa.santa_append_kv(kn, vn, rig.ks[r], rig.vs[r], rig.reps[r], rig.pt, last, nxt,
+                              stream=stream)
 
     n_app = max(rig.R, min(K, 1000))
-    sec_app, _ = timer.run(append_make, rig.R, n_app, W_, "append")
+    sec_app, _ = timer.run(append_step, rig.R, n_app, W_, "append")
     append_us = sec_app / n_app * 1e6
 
     # ---- the representatives of the whole cache (santa_build_reps, once after prefill): a
     # rebuild of every rotation copy in place from its own keys (the same values again)
-    def reps_make(n):
-        return timer.capture(lambda: [santa.santa_build_reps(rig.ks[r], rig.fill,
-                                                             reps=rig.reps[r], stream=stream)
-                                      for r in range(n)])
+    def reps_step(r):
+        santa.santa_build_reps(rig.ks[r], rig.fill, reps=rig.reps[r], stream=stream)
 
     n_rep = max(rig.R, min(K, 200))
-    sec_rep, _ = timer.run(reps_make, rig.R, n_rep, W_, "build_reps")
+    sec_rep, _ = timer.run(reps_step, rig.R, n_rep, W_, "build_reps")
     reps_us = sec_rep / n_rep * 1e6
     valid_tokens = int(rig.wl.page_fill.astype(np.int64).sum())
     reps_bytes = valid_tokens * cfg.kv_heads * d * rig.esize + rig.reps[0].numel() * 4
