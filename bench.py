@@ -9,12 +9,12 @@ Workload: the Qwen2.5-7B-shaped decode attention layer at 32K context (1 sequenc
 data.  A step is one SANTA++ decode step through santa_decode: one launch of the fused kernel
 (team scoring and sampling, then split-K Horvitz-Thompson attention over the sampled teams).
 
-value      steps/s of whole decode steps with inputs resident in HBM, K steps replayed from
-           CUDA graphs; the K/V/representative buffers rotate over R copies so that the
+value      steps/s of whole decode steps with inputs resident in HBM, K steps in one CUDA
+           graph (see timing); the K/V/representative buffers rotate over R copies so that the
            bytes touched between two uses of a copy exceed 6x the L2 size.
 roofline   the fused decode kernel (one launch per step): algorithmic bytes per launch (the
            team representatives, K and V of the sampled teams, q, out) / its mean duration
-           (CUDA events over graph-replayed launches), against the measured HBM copy bandwidth.
+           (CUDA events around the K launches), against the measured HBM copy bandwidth.
 e2e        the same steps through the C ABI with pinned host buffers: per step one call of
            santa_decode_host copies the query, page table and lengths host->device
            (StepInputs), runs the decode, copies out, draw/sampled ids, pi, |S| and the
