@@ -538,43 +538,10 @@ class Timer:
 
 def timing_event_pair():
     """Two timing events that become event-record nodes when recorded inside a graph capture
-    (torch.cuda.Event's `external` flag; older torch versions record them through the CUDA
-    runtime's cudaEventRecordWithFlags with cudaEventRecordExternal)."""
+    (torch.cuda.Event's `external` flag)."""
     import torch
-    try:
-        return (torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True))
-    except TypeError:
-        return _ExternalEvent(), _ExternalEvent()
-
-
-class _ExternalEvent:
-    """A timing event recorded as an event-record node under graph capture."""
-    _rt = None
-
-    def __init__(self):
-        import torch
-        self.ev = torch.cuda.Event(enable_timing=True)
-        self.ev.record()                             # creates the CUDA event
-        torch.cuda.synchronize()
-
-    def record(self, stream):
-        if _ExternalEvent._rt is None:
-            import glob
-            import torch
-            names = sorted(glob.glob(os.path.join(os.path.dirname(torch.__file__), "lib",
-                                                  "libcudart.so*")) +
-                           glob.glob("/usr/local/cuda/lib64/libcudart.so*"))
-            rt = ctypes.CDLL(names[0])
-            rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
-                                                    ctypes.c_uint]
-            _ExternalEvent._rt = rt
-        rc = _ExternalEvent._rt.cudaEventRecordWithFlags(self.ev.cuda_event, stream.cuda_stream, 1)
-        if rc:
-            raise RuntimeError(f"cudaEventRecordWithFlags: {rc}")
-
-    def elapsed_time(self, other):
-        return self.ev.elapsed_time(other.ev)
+    return (torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True))
 
 
 def measure_workload(rig, timer, lib, K, W_, peak, draws=None, dense_s=None, sampler="iid_ht",
