@@ -341,6 +341,15 @@ int santa_decode_host(const santa_decode_args* a, const void* host_in, void* dev
                       void* stream);
 
 /*
+ * santa_host_copy_route — how santa_decode_host would move `bytes` between the host buffer
+ * `host` and the device buffer `dev` (either direction): 1 when its own copy kernel would
+ * (`host` page-locked, reached by the current device at the same address, [host, host +
+ * bytes) inside one allocation, both pointers and the size multiples of 16), 0 when
+ * cudaMemcpyAsync would (also for null pointers or bytes = 0).  Enqueues nothing.
+ */
+int santa_host_copy_route(const void* host, const void* dev, size_t bytes);
+
+/*
  * santa_attend_vs — santa_attend with value-row sampling inside every listed team, in place
  * of the full P.V product ([SANTA] "Stochastic Sparse Attention for Memory-Bound
  * Inference", abstract: draw value rows from the post-softmax distribution and gather-add

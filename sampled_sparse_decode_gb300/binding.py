@@ -78,6 +78,7 @@ def lib():
             "santa_dense_decode": (i32, [A, vp]),
             "santa_decode_noalloc": (i32, [A, vp]),
             "santa_decode_host": (i32, [A, vp, vp, sz, vp, vp, sz, vp]),
+            "santa_host_copy_route": (i32, [vp, vp, sz]),
             "santa_decode_plan": (i32, [A, i32, vp]),
             "santa_decode_path": (i32, [A]),
             "santa_noalloc_scratch_bytes": (sz, []),

@@ -13,11 +13,31 @@
 
 namespace {
 
-// `host` itself, if it is page-locked memory that the current device reaches at the same
-// address (unified addressing) and the copy with `dev` can move 16-byte words (both pointers
-// and the size multiples of 16); otherwise nullptr, and santa_decode_host uses the copy
-// engine.  Pageable memory, memory pinned for another device and unaligned copies all take
-// the copy engine.
+// The driver's allocation id of a pointer into memory from a CUDA allocation API (0 if the
+// driver does not know the pointer).
+unsigned long long allocation_id(const void* ptr) {
+  static std::once_flag once;
+  static PFN_cuPointerGetAttribute_v4000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 4000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuPointerGetAttribute_v4000>(f);
+  });
+  unsigned long long id = 0;
+  if (!fn || fn(&id, CU_POINTER_ATTRIBUTE_BUFFER_ID, reinterpret_cast<CUdeviceptr>(ptr)) !=
+                 CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// `host` itself, if [host, host + bytes) lies in one page-locked allocation that the current
+// device reaches at the same address (unified addressing) and the copy with `dev` can move
+// 16-byte words (both pointers and the size multiples of 16); otherwise nullptr, and
+// santa_decode_host uses the copy engine.  Pageable memory, memory pinned for another device,
+// a range that leaves its allocation and unaligned copies all take the copy engine.
 const void* mapped_host(const void* host, const void* dev, size_t bytes) {
   if (((reinterpret_cast<uintptr_t>(host) | reinterpret_cast<uintptr_t>(dev) | bytes) & 15) != 0)
     return nullptr;
@@ -29,6 +49,10 @@ const void* mapped_host(const void* host, const void* dev, size_t bytes) {
   int cur = -1;
   if (at.type != cudaMemoryTypeHost || at.devicePointer != host ||
       cudaGetDevice(&cur) != cudaSuccess || at.device != cur)
+    return nullptr;
+  // the first and the last byte in the same allocation: the kernel stays inside it
+  const unsigned long long id = allocation_id(host);
+  if (id == 0 || allocation_id(static_cast<const unsigned char*>(host) + bytes - 1) != id)
     return nullptr;
   return host;  // unified addressing: the device reaches the memory at the host's address
 }
@@ -728,6 +752,10 @@ int santa_decode(const santa_decode_args* a, void* stream) {
 
 int santa_dense_decode(const santa_decode_args* a, void* stream) {
   return launch(a, santa::kModeDense, static_cast<cudaStream_t>(stream));
+}
+
+int santa_host_copy_route(const void* host, const void* dev, size_t bytes) {
+  return bytes && host && dev && mapped_host(host, dev, bytes) ? 1 : 0;
 }
 
 int santa_decode_host(const santa_decode_args* a, const void* host_in, void* dev_in,

@@ -91,6 +91,21 @@ def test_host_step_rejects_missing_buffers(lib):
     assert f(ctypes.addressof(a), 0x1000, 0x2000, 16, 0x3000, None, 16, None) == INVALID
 
 
+def test_host_copy_route_without_device_memory(lib):
+    # null pointers, no bytes, unaligned sizes and plain (not page-locked) host memory all
+    # take the copy engine; nothing is enqueued either way
+    f = lib.santa_host_copy_route
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t]
+    buf = (ctypes.c_ubyte * 4096)()
+    host = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert f(None, 0x2000, 64) == 0
+    assert f(host, None, 64) == 0
+    assert f(host, 0x2000, 0) == 0
+    assert f(host, 0x2000, 24) == 0
+    assert f(host, 0x2000, 64) == 0
+
+
 def test_reps_reject_bad_arguments_on_host(lib):
     f = lib.santa_build_reps
     f.restype = ctypes.c_int

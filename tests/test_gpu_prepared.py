@@ -136,6 +136,16 @@ def test_host_step_copy_routes_agree():
     pageable_in = torch.empty(n_in, dtype=torch.uint8)
     pageable_out = torch.empty(n_out, dtype=torch.uint8)
     assert pinned_in.data_ptr() % 16 == 0 and pinned_out.data_ptr() % 16 == 0
+    route = Bn.lib().santa_host_copy_route
+    assert route(pinned_in.data_ptr(), inp.slab.data_ptr(), n_in) == 1
+    assert route(pinned_out.data_ptr(), pbufs.outputs.data_ptr(), n_out) == 1
+    assert route(inp.host_slab.data_ptr(), inp.slab.data_ptr(), n_in) == 1
+    assert route(pageable_in.data_ptr(), inp.slab.data_ptr(), n_in) == 0
+    assert route(pinned_in.data_ptr() + 8, inp.slab.data_ptr(), n_in) == 0
+    # a range that runs past its pinned allocation takes the copy engine (nothing is copied
+    # by this query)
+    assert route(pinned_in.data_ptr(), inp.slab.data_ptr(),
+                 (pinned_in.untyped_storage().nbytes() + (1 << 20)) // 16 * 16) == 0
     rng = np.random.default_rng(11)
     for trial in range(3):
         # new query contents for every trial, through the same host storage
