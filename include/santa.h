@@ -5,7 +5,7 @@
  *   [ABS]  "SANTA++: Sampling Attention through Representative Keys" (arXiv 2609.35629),
  *          abstract, as printed on arxivdaily.com and fugumt.com.
  *   [EXP]  "SANTA++：用代表性 Key 采样把 KV cache 读带宽砍掉 80%" (papers.ananclaw.com
- *          explainer), section 三 "core method", its five-step pipeline and 3.1.
+ *          explainer), section 三 (the core method), its five-step pipeline and 3.1.
  *
  * What the library computes, for every sequence b and KV head h (a "unit"):
  *   teams      the n = ceil(seq_len/T) contiguous blocks of T cached tokens; team i is the
@@ -92,8 +92,8 @@ const char* santa_status_string(int status);
 
 /*
  * santa_build_reps — the team representative of every (page, KV head): the mean of the
- * page's valid keys.  [ABS: "the query scores one representative from each team";
- * EXP section 三 step 2 lists the mean key as one choice of representative.]
+ * page's valid keys.  [ABS, abstract: each team is represented by one key that the query
+ * scores; EXP section 三 step 2 lists the mean key as one choice of representative.]
  *
  *   k_pool      [num_pages][num_kv_heads][team_size][head_dim], dtype.
  *   page_fill   [num_pages] int32 valid-token count of each page (0..team_size), or NULL
@@ -122,9 +122,9 @@ int santa_update_reps(const void* k_pool, int dtype, int64_t num_pages, int num_
  * santa_append_kv — one decode step's new token per (sequence, KV head), written into the
  * paged cache, with the representative of its page brought up to date.  This is the step
  * on either side of the decode path: tokens arrive one at a time and the teams they land in
- * must stay described by their mean key.  [ABS: "the query scores one representative from
- * each team"; EXP section 三 step 2, mean key; section 八 on keeping teams current as the
- * sequence grows.]
+ * must stay described by their mean key.  [ABS, abstract: one representative key per team;
+ * EXP section 三 step 2, mean key; section 八 on keeping teams current as the sequence
+ * grows.]
  *
  *   k_new, v_new   [batch][num_kv_heads][head_dim], dtype (device).
  *   seq_lens       [batch] current lengths L_b (device); the token goes to position L_b:
@@ -225,8 +225,8 @@ size_t santa_decode_workspace_min_bytes(int batch, int num_q_heads, int num_kv_h
  * santa_sample — score the representatives, form the GQA-mixed team distribution, draw M
  * teams, deduplicate and compute the inclusion probabilities.  Writes draw_ids, sel_ids,
  * sel_count, pi and team_probs (if not NULL).
- * [ABS: "the query scores one representative from each team to decide which teams to
- * sample"; EXP section 三 steps 2-3.]  Uses no workspace.
+ * [ABS, abstract: the scores of the representatives decide which teams are sampled; EXP
+ * section 三 steps 2-3.]  Uses no workspace.
  */
 int santa_sample(const santa_decode_args* a, void* stream);
 
@@ -237,8 +237,8 @@ int santa_sample(const santa_decode_args* a, void* stream);
  * indices < n, any order, pi finite and > 0: the inclusion probability for Horvitz-Thompson
  * weights, M q_i / c_i for Hansen-Hurwitz ones); entries out of range set SANTA_DEV_BAD_SEL
  * and are skipped.
- * [ABS: "We compute exact attention scores within the sampled teams and reweight each
- * team's contribution by the inverse of its inclusion probability"; EXP steps 4-5.]
+ * [ABS, abstract: attention is exact inside the sampled teams, and each team's share is
+ * scaled by one over the probability that the team is in the sample; EXP steps 4-5.]
  */
 int santa_attend(const santa_decode_args* a, void* stream);
 

@@ -136,7 +136,7 @@ double oracle_uniform(uint64_t seed, int b, int h, int r) {
 /* ---------------------------------------------------------------- step 1-2: representatives */
 
 /* rep[p][h][:] = mean of the page's first fill[p] keys (fill NULL: every page full);
- * a page with no valid key gets the zero vector.  [ABS; EXP 三 step 2, "mean"]
+ * a page with no valid key gets the zero vector.  [ABS; EXP 三 step 2, the mean key]
  * Returns 0, or -1 if a fill is out of range. */
 int oracle_build_reps(const oracle_problem* pr, const int32_t* page_fill, double* reps) {
   const int d = pr->head_dim, T = pr->team_size;
@@ -255,7 +255,7 @@ void oracle_draw(const double* p, int n, int M, uint64_t seed, int b, int h, int
 }
 
 /* S = distinct drawn teams in ascending order, with pi_i = 1 - (1 - p_i)^M evaluated as
- * -expm1(M log1p(-p_i)).  Returns |S|.  [ABS "inverse of its inclusion probability"] */
+ * -expm1(M log1p(-p_i)).  Returns |S|.  [ABS, abstract: the weights 1/pi_i] */
 int oracle_select(const int32_t* draws, int M, const double* p, int n, int32_t* sel,
                   double* pi) {
   int count = 0;

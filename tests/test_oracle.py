@@ -135,7 +135,7 @@ def test_bf16_decoding_matches_torch():
 
 
 def test_reps_are_means_of_valid_keys():
-    """Representative = mean key of the team (explainer 三 step 2 "mean"), partial last
+    """Representative = mean key of the team (explainer 三 step 2: the mean key), partial last
     team averaged over its valid keys only, an empty page gives zeros."""
     cfg = _tiny(dtype="bf16", batch=2, kv_heads=2, q_heads=4, seq_len=37, paged=True,
                 num_pages=13)
@@ -246,7 +246,7 @@ def test_draws_follow_the_plain_definition_on_the_unrounded_probabilities():
     """The fixed-point draws against the method's plain definition, taken exactly: with the
     fp64 probabilities p as exact rationals, C_i = p_0 + ... + p_i, Z = C_{n-1} and
     u = (x + 1/2) / 2^32 (x the draw's Philox word), draw r is the smallest i with
-    u Z < C_i ("sample M teams with probability p_i", explainer section 三 step 3).  The
+    u Z < C_i (M teams drawn according to p, explainer section 三 step 3).  The
     62-bit rounding of p may move a draw only across a boundary that u Z lies within
     1e-12 Z of; such draws are counted and must be rare, every other draw must agree."""
     import bisect
