@@ -123,3 +123,80 @@ def test_variants_reject_shapes_sampled_across_ctas():
     santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens,
                        wl.cfg.draws, 1)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name,sampler,alpha", [
+    ("qwen7b_32k_b1_m31", "systematic", 0.05),
+    ("qwen7b_32k_b8_m64", "iid_hh", 0.0),
+    ("llama8b_paged_32k_b16_m32", "iid_ht", 0.05),
+    ("long_128k_b4_m64", "systematic", 0.0),
+])
+def test_sampler_variants_at_full_size(name, sampler, alpha):
+    """The sampler variants on the full-size workloads, in the launch shape the accuracy
+    benchmark uses (the compact form's variant instantiations).  On up to 8 units spread over
+    the batch and the heads: q, the draws (window rule), S and 1 / weight against the oracle;
+    then santa_attend on the oracle's sets and weights for those units against the oracle's
+    attention, and the whole step's outputs wherever its sets equal the oracle's."""
+    from helpers import full_oracle_reps, full_workload
+    from test_gpu_parity import spread_units
+    wl = full_workload(name)
+    cfg = wl.cfg
+    dw = DeviceWorkload(wl)
+    pr = problem(wl)
+    reps_o = full_oracle_reps(name)
+    reps = santa.santa_build_reps(dw.k_pool, dw.page_fill)
+    M, seed = cfg.draws, 2024
+    assert santa.santa_decode_path(dw.q, dw.k_pool, dw.page_table, M, sampler=sampler,
+                                   mix_alpha=alpha) == "compact"
+    bufs = santa.santa_sample(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens, M,
+                              seed, team_probs=True, sampler=sampler, mix_alpha=alpha)
+    db = santa.santa_decode(dw.q, dw.k_pool, dw.v_pool, reps, dw.page_table, dw.seq_lens, M,
+                            seed, sampler=sampler, mix_alpha=alpha)
+    torch.cuda.synchronize()
+    assert bufs.status() == 0 and db.status() == 0
+    # the whole step draws exactly what the sampling-only launch draws
+    assert torch.equal(db.draw_ids, bufs.draw_ids) and torch.equal(db.sel_count, bufs.sel_count)
+    inside = total = 0
+    sel_t, cnt_t, rc_t = bufs.sel_ids.clone(), bufs.sel_count.clone(), bufs.pi.clone()
+    units = []
+    for b, h in spread_units(cfg.batch, cfg.kv_heads):
+        q = oracle.mix(oracle.team_probs(pr, reps_o, b, h), alpha)
+        n = q.size
+        q_gpu = bufs.team_probs[b, h, :n].cpu().numpy().astype(np.float64)
+        np.testing.assert_allclose(q_gpu, q, rtol=1e-5, atol=1e-7 * q.max())
+        draws, t, C = oracle.draw_with(sampler, q, M, seed, b, h)
+        g_draws = bufs.draw_ids[b, h].cpu().numpy()
+        i, o = compare_draws(g_draws, draws, t, C)
+        assert o == 0, f"unit ({b},{h}): {o} draws differ outside the boundary window"
+        inside, total = inside + i, total + M
+        sel, rc = oracle.select_ex(draws, q, sampler)
+        cnt = int(bufs.sel_count[b, h])
+        g_sel = bufs.sel_ids[b, h].cpu().numpy()
+        g_rc = bufs.pi[b, h].cpu().numpy().astype(np.float64)
+        assert (g_sel[cnt:] == -1).all() and (g_rc[cnt:] == 0).all()
+        if np.array_equal(g_draws, draws):
+            assert np.array_equal(g_sel[:cnt], sel)
+            np.testing.assert_allclose(g_rc[:cnt], rc, rtol=TOL_PI)
+        units.append(((b, h), sel, rc))
+        sel_t[b, h] = -1
+        sel_t[b, h, :sel.size] = torch.from_numpy(sel).cuda()
+        cnt_t[b, h] = sel.size
+        rc_t[b, h] = 0.0
+        rc_t[b, h, :sel.size] = torch.from_numpy(rc.astype(np.float32)).cuda()
+    assert inside <= BOUNDARY_SHARE * total
+    ab = santa.santa_attend(dw.q, dw.k_pool, dw.v_pool, dw.page_table, dw.seq_lens, sel_t,
+                            cnt_t, rc_t)
+    torch.cuda.synchronize()
+    assert ab.status() == 0
+    G, tol = cfg.group, TOL_OUT[cfg.dtype]
+    fused = 0
+    for (b, h), sel, rc in units:
+        want = oracle.attend(pr, b, h, sel, rc)
+        got = ab.out[b, h * G:(h + 1) * G].cpu().numpy()
+        assert np.abs(got - want).max() <= tol, (b, h)
+        if int(db.sel_count[b, h]) == sel.size and np.array_equal(
+                db.sel_ids[b, h, :sel.size].cpu().numpy(), sel):
+            got = db.out[b, h * G:(h + 1) * G].cpu().numpy()
+            assert np.abs(got - want).max() <= tol, (b, h)
+            fused += 1
+    assert fused >= 1
